@@ -1,0 +1,402 @@
+"""Benchmark of the fused FP8 AdamW + DRE step on GB300.
+
+Default workload: the Llama-2-7B-shaped parameter set (6,738,415,616 params,
+G = 128), synthetic fp32 master weights and bf16 gradients (no model weights
+or data).  A step is one launch of the fused kernel over the whole flat
+buffer.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama7b]
+                  [--G 128] [--impl ours|reference]
+
+Metric: parameters updated per second (whole job), with the dominant
+kernel's achieved HBM bandwidth against the measured copy peak.
+--impl reference times the float64 CPU oracle on the host cores instead (a
+deliberately slow baseline, bounded sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 AdamW+DRE step: params/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL = "adamw_dre_step_kernel"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="llama7b")
+    p.add_argument("--G", type=int, default=128)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "coat_fp8_adamw_gb300", "csrc")
+    for name in ("adamw_dre_step.cu", "coat_device.cuh", "coat_tables.inc"):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, G: int):
+    """DRAM bytes per parameter of the step kernel from a committed ncu summary,
+    if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    digest = kernel_source_digest()
+    for line in open(p):
+        f = line.split()
+        if len(f) >= 4 and not line.startswith("#") and f[0] == digest and int(f[1]) == G:
+            return float(f[3])  # bytes per parameter
+    return None
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the float64 oracle on a bounded sample of the workload
+# ---------------------------------------------------------------------------
+def cpu_baseline(workload: str, G: int, seconds: float):
+    import numpy as np
+
+    import oracle
+    from coat_fp8_adamw_gb300 import synth
+    wl = synth.workload(workload, G)
+    sample = min(wl.n, 1 << 22)
+    rng = np.random.default_rng(0)
+    w = (rng.standard_normal(sample) * 0.02).astype(np.float32)
+    g = synth.f32_to_bf16_bits((rng.standard_normal(sample) * 1e-3).astype(np.float32))
+    mq, vq, meta = synth.random_state_np(sample, G, seed=1)
+    hp = synth.HYPER
+    threads = oracle.threads(0)
+    done, t0, step = 0, time.perf_counter(), 1
+    while True:
+        oracle.adamw_step(w, g, mq, vq, meta, G, hp["beta1"], hp["beta2"], hp["lr"], hp["eps"],
+                          hp["weight_decay"], step, nthreads=threads)
+        done += sample
+        step += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": done / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{step - 1} steps over the first {sample} params ({workload}-shaped, G={G}), "
+                      f"{el:.1f} s of float64 CPU work"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    t0 = time.perf_counter()
+    per_step = []
+    base = None
+    for i in range(args.warmup + args.steps):
+        b = cpu_baseline(args.workload, args.G, max(1.0, args.cpu_seconds / 4))
+        if i >= args.warmup:
+            per_step.append(b["value"])
+        base = b
+    value = statistics.median(per_step) if per_step else base["value"]
+    from coat_fp8_adamw_gb300 import synth
+    n = synth.workload(args.workload, args.G).n
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": n / value * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload}-shaped parameter set", "G": args.G,
+                       "params": n, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": base["cores"],
+                             "kind": "oracle", "sample": base["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": time.perf_counter() - t0}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import coat_fp8_adamw_gb300 as coat
+    from coat_fp8_adamw_gb300 import synth
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    coat.lib()  # fail loudly if the library is missing
+
+    wl = synth.workload(args.workload, args.G)
+    n, G = wl.n, wl.G
+    ng = coat.num_groups(n, G)
+    hp = synth.HYPER
+    w = synth.init_weights_torch(wl, dev)
+    g = synth.grad_torch(wl, 1, dev)
+    mq = torch.zeros(n, dtype=torch.uint8, device=dev)
+    vq = torch.zeros(n, dtype=torch.uint8, device=dev)
+    meta = torch.zeros(ng, 4, dtype=torch.float32, device=dev)
+    meta[:, 1] = 1.0
+    meta[:, 3] = 1.0
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream(dev)
+
+    def step(t):
+        coat.coat_fp8_adamw_step(w, g, mq, vq, meta, G, hp["beta1"], hp["beta2"], hp["lr"],
+                                 hp["eps"], hp["weight_decay"], t, stream=stream)
+
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        step(t)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for i in range(args.steps):
+        t += 1
+        starts[i].record(stream)
+        step(t)
+        ends[i].record(stream)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    total_ms = t_begin.elapsed_time(t_end)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    ms_per_step = total_ms / args.steps
+    value = ws * n * args.steps / (total_ms / 1e3)
+    avg_launch = statistics.mean(launch_ms)
+    bpp = coat.bytes_per_param(G)
+    achieved = bpp * n / (avg_launch / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    traffic_bpp = recorded_traffic(args.workload, G)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        e2e = e2e_leg(args, coat, synth, torch, dev, w, g, mq, vq, meta, n, G, ng, hp, t)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload, G, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic",
+                "config": {"workload": f"{args.workload}-shaped parameter set", "G": G,
+                           "params": n, "groups": ng, "bytes_per_param": bpp,
+                           "parallelism": "replicas" if ws > 1 else "single GPU",
+                           "l2": "working set %.1f GB >> 129 MB L2: no flush needed"
+                                 % (bpp * n / 1e9)},
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
+                             "unit": "GB/s", "frac": achieved / peak,
+                             "peak_kind": f"{peak_kind} (copy bandwidth)",
+                             "traffic": (traffic_bpp * n) if traffic_bpp else None,
+                             "kernel": KERNEL, "avg_launch_ms": avg_launch,
+                             "min_launch_ms": min(launch_ms), "max_launch_ms": max(launch_ms)},
+                "gpu_launches": args.steps,
+                "clocks": clk,
+                "e2e": e2e,
+                "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e_leg(args, coat, synth, torch, dev, w, g, mq, vq, meta, n, G, ng, hp, t):
+    """Same step through the public API with the state and gradient in pinned
+    host memory: each step copies w, g, codes and meta to the device, runs the
+    C-ABI step, and copies w, codes and meta back.  The whole state is streamed
+    in chunks through two device staging sets so that copies in both
+    directions overlap the kernel."""
+    chunk = min(n, 1 << 28)  # params per chunk (multiple of 256)
+    try:
+        hw = torch.empty(n, dtype=torch.float32, pin_memory=True)
+        hg = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+        hmq = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        hvq = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        hmeta = torch.empty(ng, 4, dtype=torch.float32, pin_memory=True)
+    except RuntimeError as e:
+        return {"error": f"pinned host allocation failed: {e}"}
+    hw.copy_(w)
+    hg.copy_(g)
+    hmq.copy_(mq)
+    hvq.copy_(vq)
+    hmeta.copy_(meta)
+    cg = chunk // G
+    bufs = []
+    for _ in range(2):
+        bufs.append((torch.empty(chunk, dtype=torch.float32, device=dev),
+                     torch.empty(chunk, dtype=torch.bfloat16, device=dev),
+                     torch.empty(chunk, dtype=torch.uint8, device=dev),
+                     torch.empty(chunk, dtype=torch.uint8, device=dev),
+                     torch.empty(cg, 4, dtype=torch.float32, device=dev)))
+    streams = [torch.cuda.Stream(dev) for _ in range(2)]
+
+    def one_step(step_t):
+        for ci, a in enumerate(range(0, n, chunk)):
+            b = min(n, a + chunk)
+            m = b - a
+            ga, gb = a // G, (b + G - 1) // G
+            s = streams[ci % 2]
+            dw, dg, dm, dv, dmeta = bufs[ci % 2]
+            with torch.cuda.stream(s):
+                dw[:m].copy_(hw[a:b], non_blocking=True)
+                dg[:m].copy_(hg[a:b], non_blocking=True)
+                dm[:m].copy_(hmq[a:b], non_blocking=True)
+                dv[:m].copy_(hvq[a:b], non_blocking=True)
+                dmeta[:gb - ga].copy_(hmeta[ga:gb], non_blocking=True)
+                coat.coat_fp8_adamw_step(dw[:m], dg[:m], dm[:m], dv[:m], dmeta[:gb - ga], G,
+                                         hp["beta1"], hp["beta2"], hp["lr"], hp["eps"],
+                                         hp["weight_decay"], step_t, stream=s)
+                hw[a:b].copy_(dw[:m], non_blocking=True)
+                hmq[a:b].copy_(dm[:m], non_blocking=True)
+                hvq[a:b].copy_(dv[:m], non_blocking=True)
+                hmeta[ga:gb].copy_(dmeta[:gb - ga], non_blocking=True)
+        for s in streams:
+            s.synchronize()
+
+    one_step(t + 1)  # warm-up
+    t0 = time.perf_counter()
+    for i in range(args.e2e_steps):
+        one_step(t + 2 + i)
+    el = time.perf_counter() - t0
+    h2d = n * (4 + 2 + 1 + 1) + ng * 16
+    d2h = n * (4 + 1 + 1) + ng * 16
+    return {"value": n * args.e2e_steps / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "chunk_params": chunk,
+            "note": "state and gradient in pinned host memory, streamed through the C-ABI "
+                    "step in chunks on two streams; host wall clock"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+"""Python binding of libcoat_gb300 (the C ABI declared in include/coat.h).
+
+This module only marshals arguments: it checks tensor dtypes, devices and
+shapes, passes raw device pointers and the current CUDA stream through
+ctypes, and turns a non-zero status into :class:`CoatError`.  Every step of
+the optimizer runs in the library's CUDA kernels.  There is no CPU or PyTorch
+fallback: if the shared library has not been built, every call raises.
+
+Build it with ``python -c "import __graft_entry__ as g; g.build()"`` (or
+``python coat_fp8_adamw_gb300/_build.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+from . import _build
+
+__all__ = ["CoatError", "coat_fp8_adamw_step", "coat_dre_quantize", "coat_dre_dequantize",
+           "coat_status_string", "coat_r_e4m3", "coat_version", "lib", "lib_path",
+           "num_groups", "bytes_per_param", "STATUS"]
+
+STATUS = {0: "COAT_OK", 1: "COAT_ERR_INVALID_ARG", 2: "COAT_ERR_MISALIGNED",
+          3: "COAT_ERR_UNSUPPORTED_G", 4: "COAT_ERR_CUDA", 5: "COAT_ERR_NOT_DEVICE"}
+
+#: symbols the shared library must export (one per declaration in include/coat.h)
+EXPORTS = ("coat_fp8_adamw_step", "coat_dre_quantize", "coat_dre_dequantize",
+           "coat_status_string", "coat_r_e4m3", "coat_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CoatError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = coat_status_string(status) if _lib is not None else STATUS.get(status, "?")
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({msg})")
+
+
+def lib_path() -> str:
+    return _build.lib_path()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises if it has not been built: no fallback exists."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libcoat_gb300 is not built ({path} missing); run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        L = ctypes.CDLL(path)
+        vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        L.coat_fp8_adamw_step.argtypes = [vp, vp, vp, vp, vp, i64, i32, f32, f32, f32, f32, f32,
+                                          i64, vp]
+        L.coat_fp8_adamw_step.restype = ctypes.c_int
+        L.coat_dre_quantize.argtypes = [vp, i64, i32, vp, vp, vp, vp]
+        L.coat_dre_quantize.restype = ctypes.c_int
+        L.coat_dre_dequantize.argtypes = [vp, vp, vp, i64, i32, vp, vp]
+        L.coat_dre_dequantize.restype = ctypes.c_int
+        L.coat_status_string.argtypes = [ctypes.c_int]
+        L.coat_status_string.restype = ctypes.c_char_p
+        L.coat_r_e4m3.argtypes = []
+        L.coat_r_e4m3.restype = ctypes.c_double
+        L.coat_version.argtypes = []
+        L.coat_version.restype = ctypes.c_int32
+        _lib = L
+        return L
+
+
+def coat_status_string(status: int) -> str:
+    return lib().coat_status_string(int(status)).decode()
+
+
+def coat_r_e4m3() -> float:
+    return float(lib().coat_r_e4m3())
+
+
+def coat_version() -> int:
+    return int(lib().coat_version())
+
+
+def num_groups(n: int, G: int) -> int:
+    return (n + G - 1) // G
+
+
+def bytes_per_param(G: int) -> float:
+    """Algorithmic HBM traffic of one step per parameter (read + write).
+
+    w fp32 read+write 8 B, g bf16 read 2 B, m and v codes read+write 4 B, and
+    the 16-byte (S_m, k_m, S_v, k_v) record of each group read+write 32/G B.
+    """
+    return 14.0 + 32.0 / G
+
+
+# ---------------------------------------------------------------------------
+# torch-tensor front end
+# ---------------------------------------------------------------------------
+
+def _stream_ptr(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(t, dtype, numel: int, name: str, device=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t.data_ptr()
+
+
+def coat_fp8_adamw_step(w, g, m_q, v_q, meta, G: int, beta1: float, beta2: float, lr: float,
+                        eps: float, weight_decay: float, step: int, stream=None) -> None:
+    """One fused FP8 AdamW + DRE step, in place on w, m_q, v_q and meta.
+
+    w fp32 [n]; g bf16 [n]; m_q, v_q uint8 [n]; meta fp32 [ceil(n/G), 4]
+    holding (S_m, k_m, S_v, k_v) per group.  Runs on ``stream`` (default: the
+    current torch stream) and returns without synchronizing.
+    """
+    import torch
+    n = w.numel()
+    dev = w.device
+    pw = _check(w, torch.float32, n, "w")
+    pg = _check(g, torch.bfloat16, n, "g", dev)
+    pm = _check(m_q, torch.uint8, n, "m_q", dev)
+    pv = _check(v_q, torch.uint8, n, "v_q", dev)
+    pmeta = _check(meta, torch.float32, 4 * num_groups(n, G), "meta", dev)
+    st = lib().coat_fp8_adamw_step(pw, pg, pm, pv, pmeta, n, int(G), float(beta1), float(beta2),
+                                   float(lr), float(eps), float(weight_decay), int(step),
+                                   _stream_ptr(stream))
+    if st != 0:
+        raise CoatError(st, "coat_fp8_adamw_step")
+
+
+def coat_dre_quantize(x, G: int, q, scale, k, stream=None) -> None:
+    """DRE + E4M3 quantization: x fp32 [n] -> q uint8 [n], scale/k fp32 [ceil(n/G)]."""
+    import torch
+    n = x.numel()
+    ng = num_groups(n, G)
+    px = _check(x, torch.float32, n, "x")
+    pq = _check(q, torch.uint8, n, "q", x.device)
+    ps = _check(scale, torch.float32, ng, "scale", x.device)
+    pk = _check(k, torch.float32, ng, "k", x.device)
+    st = lib().coat_dre_quantize(px, n, int(G), pq, ps, pk, _stream_ptr(stream))
+    if st != 0:
+        raise CoatError(st, "coat_dre_quantize")
+
+
+def coat_dre_dequantize(q, scale, k, G: int, x, stream=None) -> None:
+    """Inverse of :func:`coat_dre_quantize`: x = sign(q)(|E4M3(q)| scale)^(1/k)."""
+    import torch
+    n = q.numel()
+    ng = num_groups(n, G)
+    pq = _check(q, torch.uint8, n, "q")
+    ps = _check(scale, torch.float32, ng, "scale", q.device)
+    pk = _check(k, torch.float32, ng, "k", q.device)
+    px = _check(x, torch.float32, n, "x", q.device)
+    st = lib().coat_dre_dequantize(pq, ps, pk, n, int(G), px, _stream_ptr(stream))
+    if st != 0:
+        raise CoatError(st, "coat_dre_dequantize")

@@ -1,0 +1,136 @@
+// coat_abi.cu -- the extern "C" entry points declared in include/coat.h:
+// argument validation, per-launch constants (bias corrections), and the
+// dispatch to the templated kernels.  No allocation, no state, no host sync.
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "coat.h"
+#include "coat_kernels.h"
+
+namespace {
+
+bool pow2_group(int32_t G) { return G >= 1 && G <= 256 && (G & (G - 1)) == 0; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// Device (or managed) memory of the current context.  Host memory is refused
+// even where the GPU could reach it, since the kernels assume HBM.
+bool is_device(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error state of this query
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+coat_status from_cuda(cudaError_t e) { return e == cudaSuccess ? COAT_OK : COAT_ERR_CUDA; }
+
+int64_t num_groups(int64_t n, int32_t G) { return (n + G - 1) / G; }
+
+}  // namespace
+
+extern "C" {
+
+coat_status coat_fp8_adamw_step(float* w, const uint16_t* g, uint8_t* m_q, uint8_t* v_q,
+                                coat_group_meta* meta, int64_t n, int32_t G, float beta1,
+                                float beta2, float lr, float eps, float weight_decay,
+                                int64_t step, void* stream) {
+    if (!w || !g || !m_q || !v_q || !meta || n < 1 || step < 1) return COAT_ERR_INVALID_ARG;
+    if (!pow2_group(G)) return COAT_ERR_UNSUPPORTED_G;
+    if (!aligned16(w) || !aligned16(g) || !aligned16(m_q) || !aligned16(v_q) || !aligned16(meta))
+        return COAT_ERR_MISALIGNED;
+    if (!std::isfinite(beta1) || !std::isfinite(beta2) || !std::isfinite(lr) ||
+        !std::isfinite(eps) || !std::isfinite(weight_decay) || beta1 < 0.0f || beta1 >= 1.0f ||
+        beta2 < 0.0f || beta2 >= 1.0f || lr < 0.0f || !(eps > 0.0f) || weight_decay < 0.0f)
+        return COAT_ERR_INVALID_ARG;
+    const size_t nb = (size_t)n;
+    const size_t ng = (size_t)num_groups(n, G);
+    if (overlaps(g, 2 * nb, w, 4 * nb) || overlaps(g, 2 * nb, m_q, nb) ||
+        overlaps(g, 2 * nb, v_q, nb) || overlaps(g, 2 * nb, meta, 16 * ng) ||
+        overlaps(w, 4 * nb, m_q, nb) || overlaps(w, 4 * nb, v_q, nb) ||
+        overlaps(w, 4 * nb, meta, 16 * ng) || overlaps(m_q, nb, v_q, nb) ||
+        overlaps(m_q, nb, meta, 16 * ng) || overlaps(v_q, nb, meta, 16 * ng))
+        return COAT_ERR_INVALID_ARG;
+    if (!is_device(w) || !is_device(g) || !is_device(m_q) || !is_device(v_q) || !is_device(meta))
+        return COAT_ERR_NOT_DEVICE;
+
+    // bias corrections 1 - beta^t, once per launch, in double
+    const double b1 = beta1, b2 = beta2;
+    const double bc1 = 1.0 - std::pow(b1, (double)step);
+    const double bc2 = 1.0 - std::pow(b2, (double)step);
+    if (!(bc1 > 0.0) || !(bc2 > 0.0)) return COAT_ERR_INVALID_ARG;  // beta == 0 is fine: bc = 1
+
+    coat::StepArgs a;
+    a.w = w;
+    a.g = g;
+    a.mq = m_q;
+    a.vq = v_q;
+    a.meta = reinterpret_cast<float4*>(meta);
+    a.n = n;
+    a.beta1 = beta1;
+    a.beta2 = beta2;
+    a.omb1 = (float)(1.0 - b1);
+    a.omb2 = (float)(1.0 - b2);
+    a.c1 = (float)((double)lr / bc1);
+    a.c2 = (float)(1.0 / bc2);
+    a.eps = eps;
+    a.decay = (float)(1.0 - (double)lr * (double)weight_decay);
+    return from_cuda(coat::launch_adamw_dre_step(a, G, static_cast<cudaStream_t>(stream)));
+}
+
+coat_status coat_dre_quantize(const float* x, int64_t n, int32_t G, uint8_t* q, float* scale,
+                              float* k, void* stream) {
+    if (!x || !q || !scale || !k || n < 1) return COAT_ERR_INVALID_ARG;
+    if (!pow2_group(G)) return COAT_ERR_UNSUPPORTED_G;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scale) || !aligned16(k))
+        return COAT_ERR_MISALIGNED;
+    const size_t nb = (size_t)n, ng = (size_t)num_groups(n, G);
+    if (overlaps(x, 4 * nb, q, nb) || overlaps(x, 4 * nb, scale, 4 * ng) ||
+        overlaps(x, 4 * nb, k, 4 * ng) || overlaps(q, nb, scale, 4 * ng) ||
+        overlaps(q, nb, k, 4 * ng) || overlaps(scale, 4 * ng, k, 4 * ng))
+        return COAT_ERR_INVALID_ARG;
+    if (!is_device(x) || !is_device(q) || !is_device(scale) || !is_device(k))
+        return COAT_ERR_NOT_DEVICE;
+    coat::QuantArgs a{x, q, scale, k, n};
+    return from_cuda(coat::launch_dre_quantize(a, G, static_cast<cudaStream_t>(stream)));
+}
+
+coat_status coat_dre_dequantize(const uint8_t* q, const float* scale, const float* k, int64_t n,
+                                int32_t G, float* x, void* stream) {
+    if (!x || !q || !scale || !k || n < 1) return COAT_ERR_INVALID_ARG;
+    if (!pow2_group(G)) return COAT_ERR_UNSUPPORTED_G;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scale) || !aligned16(k))
+        return COAT_ERR_MISALIGNED;
+    const size_t nb = (size_t)n, ng = (size_t)num_groups(n, G);
+    if (overlaps(x, 4 * nb, q, nb) || overlaps(x, 4 * nb, scale, 4 * ng) ||
+        overlaps(x, 4 * nb, k, 4 * ng))
+        return COAT_ERR_INVALID_ARG;
+    if (!is_device(x) || !is_device(q) || !is_device(scale) || !is_device(k))
+        return COAT_ERR_NOT_DEVICE;
+    coat::DequantArgs a{q, scale, k, x, n};
+    return from_cuda(coat::launch_dre_dequantize(a, G, static_cast<cudaStream_t>(stream)));
+}
+
+const char* coat_status_string(coat_status s) {
+    switch (s) {
+        case COAT_OK: return "ok";
+        case COAT_ERR_INVALID_ARG: return "invalid argument";
+        case COAT_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case COAT_ERR_UNSUPPORTED_G: return "group size must be a power of two in [1, 256]";
+        case COAT_ERR_CUDA: return "CUDA launch or runtime error";
+        case COAT_ERR_NOT_DEVICE: return "pointer is not device memory";
+    }
+    return "unknown status";
+}
+
+double coat_r_e4m3(void) { return 448.0 * 512.0; }
+
+int32_t coat_version(void) { return 100; }
+
+}  // extern "C"

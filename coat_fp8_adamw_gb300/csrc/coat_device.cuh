@@ -1,0 +1,193 @@
+// coat_device.cuh -- device-side building blocks shared by the GB300 kernels:
+// FP8 E4M3 packing, base-2 exp/log through the SFU, per-group Dynamic Range
+// Expansion parameters, and the 128-bit streaming loads/stores.
+//
+// Method: COAT paper-review page (xllm-io), section 3 core formulas --
+//   FP8 quantization  X_FP8 = round(X / S), S = max|X| / 448
+//   expansion         f(x) = sign(x)|x|^k, R_X = max|X| / min|X|,
+//                     k = log_{R_X}(R_E4M3)
+// with the library's readings: min over non-zero |x|, k <= 8, S kept in
+// [2^-125, 2^126], R_E4M3 = 448 / 2^-9, round-to-nearest-even saturating
+// encoding.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "coat_tables.inc"
+
+namespace coat {
+
+constexpr int kVec = 16;         // elements per thread: one 128-bit load of codes
+constexpr int kThreads = 256;    // threads per CTA
+
+// log2(448), log2(R_E4M3) = log2(448 * 2^9), the k cap, and the S-range guard
+// numerators (log2 448 - 125, log2 448 + 126), as float constants.
+constexpr float kLog2_448 = 8.8073549220576041f;
+constexpr float kLog2_448_minus9 = -0.19264507794239588f;  // log2(448) - 9
+constexpr float kLog2R = 17.807354922057604f;
+constexpr float kKCap = 8.0f;
+constexpr float kGuardLo = 8.8073549220576041f - 125.0f;
+constexpr float kGuardHi = 8.8073549220576041f + 126.0f;
+
+// ---------------------------------------------------------------------------
+// SFU approximations, as documented PTX instructions (no flush-to-zero)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float sqrt_approx(float x) {
+    float y;
+    asm("sqrt.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Two fp32 values -> two E4M3 codes (round to nearest even, saturate to
+// +-448), packed little-endian: lo -> bits 0..7, hi -> bits 8..15.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------------------
+// 128-bit streaming memory access (evict-first: the data set exceeds L2)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 ld_cs(const float4* p) { return __ldcs(p); }
+__device__ __forceinline__ uint4 ld_cs(const uint4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_cs(float4* p, float4 v) { __stcs(p, v); }
+__device__ __forceinline__ void st_cs(uint4* p, uint4 v) { __stcs(p, v); }
+
+// ---------------------------------------------------------------------------
+// x > 0 finite (normal or subnormal): x = 2^e * u with u in [1, 2).
+// Returns e as an exactly representable float and log2(u) in [0, 1).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void split_log2(float x, float& e, float& log2u) {
+    uint32_t b = __float_as_uint(x);
+    int ex = (int)((b >> 23) & 0xFFu);
+    if (ex == 0) {  // subnormal: scale by 2^24 (exact)
+        b = __float_as_uint(x * 16777216.0f);
+        ex = (int)((b >> 23) & 0xFFu) - 24;
+    }
+    const float u = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
+    e = (float)(ex - 127);
+    log2u = log2f(u);
+}
+
+// 2^(hi + lo) for |lo| small, hi any finite value, with the integer part of hi
+// applied exactly.
+__device__ __forceinline__ float exp2_split(float hi, float lo) {
+    const float n = rintf(hi);
+    float f = (hi - n) + lo;           // hi - n is exact
+    const float n2 = rintf(f);
+    f -= n2;
+    return ldexpf(exp2f(f), (int)(n + n2));
+}
+
+// Parameters that turn a stored (S, k) into dequantized values:
+//   x = sign(q) * P * 2^(L(q) / k),  P = (448 S)^(1/k),  L(q) = log2(|E4M3(q)|/448)
+struct DequantParams {
+    float P;   // (448 S)^(1/k): the magnitude code 0x7E dequantizes to exactly P
+    float rk;  // 1/k
+};
+
+__device__ __forceinline__ DequantParams dequant_params(float S, float k) {
+    DequantParams d;
+    const float rk = __frcp_rn(k);
+    d.rk = rk;
+    if (!(S > 0.0f)) {
+        d.P = 0.0f;
+        return d;
+    }
+    // log2(448 S) = (e + 9) + (log2 u + log2(448) - 9)   [integer + small]
+    float e, l;
+    split_log2(S, e, l);
+    const float nhi = e + 9.0f;                    // exact integer
+    const float nlo = l + kLog2_448_minus9;        // in [-0.2, 0.81)
+    const float rk_lo = __fmul_rn(fmaf(-k, rk, 1.0f), rk);  // 1/k = rk + rk_lo
+    // t = (nhi + nlo) * (rk + rk_lo)
+    const float p = __fmul_rn(nhi, rk);
+    const float pe = fmaf(nhi, rk, -p);            // exact product error
+    const float tlo = fmaf(nlo, rk, fmaf(nhi, rk_lo, pe));
+    d.P = exp2_split(p, tlo);
+    return d;
+}
+
+// Fresh per-group parameters from the group's max and smallest non-zero
+// magnitude (section 3: R_X = max/min, k = log_{R_X} R_E4M3, S = max|f(X)|/448
+// = max^k / 448), with the library's cap and S-range guard.
+struct QuantParams {
+    float k;
+    float S;
+    float inv_mx;  // 1/max (0 for an all-zero group)
+};
+
+__device__ __forceinline__ QuantParams quant_params(float mx, float mn) {
+    QuantParams q;
+    if (!(mx > 0.0f)) {
+        q.k = 1.0f;
+        q.S = 0.0f;
+        q.inv_mx = 0.0f;
+        return q;
+    }
+    float em, lm;
+    split_log2(mx, em, lm);
+    float k = 1.0f;
+    if (mn < mx) {
+        float en, ln;
+        split_log2(mn, en, ln);
+        const float D = (em - en) + (lm - ln);   // log2(R_X) > 0
+        k = fminf(__fdiv_rn(kLog2R, D), kKCap);
+    }
+    const float L = em + lm;                     // log2(max)
+    if (L < 0.0f)
+        k = fminf(k, __fdiv_rn(kGuardLo, L));
+    else if (L > 0.0f)
+        k = fminf(k, __fdiv_rn(kGuardHi, L));
+    // S = 2^(k em + k lm - log2 448), with k*em split exactly
+    const float p = __fmul_rn(k, em);
+    const float pe = fmaf(k, em, -p);
+    const float slo = fmaf(k, lm, pe) - kLog2_448;
+    q.k = k;
+    q.S = exp2_split(p, slo);
+    q.inv_mx = __frcp_rn(mx);
+    return q;
+}
+
+// Dequantize one code: sign(q) * P * 2^(L(q) * rk).
+__device__ __forceinline__ float dequant_one(const float* s_log_tab, uint32_t code, float P,
+                                             float rk) {
+    const float L = s_log_tab[code & 0x7Fu];
+    const float mag = __fmul_rn(P, ex2_approx(__fmul_rn(L, rk)));
+    return __uint_as_float(__float_as_uint(mag) | ((code & 0x80u) << 24));
+}
+
+// Scaled, expanded value y = 448 sign(x) (|x| / max)^k, ready for E4M3 rounding.
+// `r` is |x| / max (computed by the caller), `x` supplies the sign.  A zero
+// input gives +0 (never a negative-zero code).
+__device__ __forceinline__ float expand_scaled(float x, float r, float k) {
+    const float y = ex2_approx(fmaf(k, lg2_approx(r), kLog2_448));
+    return __fadd_rn(copysignf(y, x), 0.0f);
+}
+
+// Smallest-non-zero tracking: fp32 magnitudes as unsigned bits minus one, so
+// that zero wraps to 0xFFFFFFFF and never wins a min.
+__device__ __forceinline__ uint32_t nz_key(float a) { return __float_as_uint(a) - 1u; }
+__device__ __forceinline__ float nz_key_value(uint32_t key) { return __uint_as_float(key + 1u); }
+
+}  // namespace coat

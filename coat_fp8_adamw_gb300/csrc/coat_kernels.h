@@ -1,0 +1,45 @@
+// coat_kernels.h -- internal launch interface between the C ABI (coat_abi.cu)
+// and the kernels.  Not part of the public header.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace coat {
+
+struct StepArgs {
+    float* w;
+    const uint16_t* g;
+    uint8_t* mq;
+    uint8_t* vq;
+    float4* meta;
+    int64_t n;
+    float beta1, beta2;
+    float omb1, omb2;  // 1 - beta (exact in fp32 for beta in [0.5, 1))
+    float c1;          // lr / (1 - beta1^t)
+    float c2;          // 1 / (1 - beta2^t)
+    float eps;
+    float decay;       // 1 - lr * weight_decay
+};
+
+struct QuantArgs {
+    const float* x;
+    uint8_t* q;
+    float* scale;
+    float* k;
+    int64_t n;
+};
+
+struct DequantArgs {
+    const uint8_t* q;
+    const float* scale;
+    const float* k;
+    float* x;
+    int64_t n;
+};
+
+cudaError_t launch_adamw_dre_step(const StepArgs& a, int G, cudaStream_t stream);
+cudaError_t launch_dre_quantize(const QuantArgs& a, int G, cudaStream_t stream);
+cudaError_t launch_dre_dequantize(const DequantArgs& a, int G, cudaStream_t stream);
+
+}  // namespace coat

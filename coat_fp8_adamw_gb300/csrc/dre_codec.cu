@@ -1,0 +1,191 @@
+// dre_codec.cu -- standalone Dynamic Range Expansion quantizer / dequantizer
+// for one fp32 tensor (COAT paper-review page, section 3: FP8 quantization
+// equation and the Dynamic Range Expansion equations).  Same thread layout and
+// per-group arithmetic as the fused step: 16 elements per thread, a group of
+// G >= 16 spans G/16 adjacent lanes, two-stage max / smallest-non-zero
+// reduction (per thread, then warp shuffles).
+#include "coat_kernels.h"
+#include "coat_device.cuh"
+
+namespace coat {
+
+namespace {
+
+template <int G>
+struct Geom {
+    static constexpr int kLanes = G >= kVec ? G / kVec : 1;
+    static constexpr int kGroups = G >= kVec ? 1 : kVec / G;
+    static constexpr int kElems = G >= kVec ? kVec : G;
+};
+
+template <int G>
+__global__ void __launch_bounds__(kThreads)
+dre_quantize_kernel(const QuantArgs a) {
+    using Gm = Geom<G>;
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t base = tid * kVec;
+    if (__all_sync(0xFFFFFFFFu, base >= a.n)) return;
+    const bool active = base < a.n;
+    const bool full = base + kVec <= a.n;
+
+    float x[kVec];
+    if (active && full) {
+        const float4* xp = reinterpret_cast<const float4*>(a.x + base);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 t = ld_cs(xp + i);
+            x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) x[e] = (active && base + e < a.n) ? a.x[base + e] : 0.0f;
+    }
+
+    float mx[Gm::kGroups];
+    uint32_t mn[Gm::kGroups];
+#pragma unroll
+    for (int j = 0; j < Gm::kGroups; ++j) { mx[j] = 0.0f; mn[j] = 0xFFFFFFFFu; }
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+        const int j = e / Gm::kElems;
+        const float ax = fabsf(x[e]);
+        mx[j] = fmaxf(mx[j], ax);
+        mn[j] = min(mn[j], nz_key(ax));
+    }
+#pragma unroll
+    for (int off = Gm::kLanes / 2; off > 0; off >>= 1) {
+        mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xFFFFFFFFu, mx[0], off));
+        mn[0] = min(mn[0], __shfl_xor_sync(0xFFFFFFFFu, mn[0], off));
+    }
+    QuantParams qp[Gm::kGroups];
+    float pre[Gm::kGroups];
+#pragma unroll
+    for (int j = 0; j < Gm::kGroups; ++j) {
+        qp[j] = quant_params(mx[j], nz_key_value(mn[j]));
+        pre[j] = 1.0f;
+        if (mx[j] > 0.0f && mx[j] < 1.17549435e-38f) {
+            pre[j] = 16777216.0f;
+            qp[j].inv_mx = __frcp_rn(mx[j] * 16777216.0f);
+        }
+    }
+    if (!active) return;
+
+    uint32_t out[kVec / 4];
+#pragma unroll
+    for (int e = 0; e < kVec; e += 2) {
+        const int j0 = e / Gm::kElems, j1 = (e + 1) / Gm::kElems;
+        const float r0 = (fabsf(x[e]) * pre[j0]) * qp[j0].inv_mx;
+        const float r1 = (fabsf(x[e + 1]) * pre[j1]) * qp[j1].inv_mx;
+        const uint32_t p = e4m3x2(expand_scaled(x[e], r0, qp[j0].k), expand_scaled(x[e + 1], r1, qp[j1].k));
+        if ((e & 2) == 0) out[e / 4] = p; else out[e / 4] |= p << 16;
+    }
+    if (full) {
+        st_cs(reinterpret_cast<uint4*>(a.q + base), make_uint4(out[0], out[1], out[2], out[3]));
+    } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e)
+            if (base + e < a.n) a.q[base + e] = (uint8_t)(out[e / 4] >> (8 * (e & 3)));
+    }
+    const int64_t g0 = base / G;
+    const bool leader = G >= kVec ? ((base % G) == 0) : true;
+    if (leader) {
+#pragma unroll
+        for (int j = 0; j < Gm::kGroups; ++j)
+            if ((g0 + j) * G < a.n) { a.scale[g0 + j] = qp[j].S; a.k[g0 + j] = qp[j].k; }
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads)
+dre_dequantize_kernel(const DequantArgs a) {
+    using Gm = Geom<G>;
+    __shared__ float s_log[128];
+    if (threadIdx.x < 128) s_log[threadIdx.x] = __uint_as_float(kLog2Frac448Hi[threadIdx.x]);
+    __syncthreads();
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t base = tid * kVec;
+    if (base >= a.n) return;
+    const bool full = base + kVec <= a.n;
+    uint32_t q[kVec / 4];
+    if (full) {
+        const uint4 t = ld_cs(reinterpret_cast<const uint4*>(a.q + base));
+        q[0] = t.x; q[1] = t.y; q[2] = t.z; q[3] = t.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < kVec / 4; ++i) q[i] = 0u;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e)
+            if (base + e < a.n) q[e / 4] |= (uint32_t)a.q[base + e] << (8 * (e & 3));
+    }
+    const int64_t g0 = base / G;
+    DequantParams d[Gm::kGroups];
+#pragma unroll
+    for (int j = 0; j < Gm::kGroups; ++j) {
+        float S = 0.0f, k = 1.0f;
+        if ((g0 + j) * G < a.n) { S = a.scale[g0 + j]; k = a.k[g0 + j]; }
+        d[j] = dequant_params(S, k);
+    }
+    float x[kVec];
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+        const int j = e / Gm::kElems;
+        x[e] = dequant_one(s_log, (q[e / 4] >> (8 * (e & 3))) & 0xFFu, d[j].P, d[j].rk);
+    }
+    if (full) {
+        float4* xp = reinterpret_cast<float4*>(a.x + base);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) st_cs(xp + i, make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]));
+    } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e)
+            if (base + e < a.n) a.x[base + e] = x[e];
+    }
+}
+
+template <int G>
+cudaError_t launch_q(const QuantArgs& a, cudaStream_t s) {
+    const int64_t threads = (a.n + kVec - 1) / kVec;
+    dre_quantize_kernel<G><<<(unsigned)((threads + kThreads - 1) / kThreads), kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int G>
+cudaError_t launch_dq(const DequantArgs& a, cudaStream_t s) {
+    const int64_t threads = (a.n + kVec - 1) / kVec;
+    dre_dequantize_kernel<G><<<(unsigned)((threads + kThreads - 1) / kThreads), kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dre_quantize(const QuantArgs& a, int G, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_q<1>(a, s);
+        case 2: return launch_q<2>(a, s);
+        case 4: return launch_q<4>(a, s);
+        case 8: return launch_q<8>(a, s);
+        case 16: return launch_q<16>(a, s);
+        case 32: return launch_q<32>(a, s);
+        case 64: return launch_q<64>(a, s);
+        case 128: return launch_q<128>(a, s);
+        case 256: return launch_q<256>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_dre_dequantize(const DequantArgs& a, int G, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_dq<1>(a, s);
+        case 2: return launch_dq<2>(a, s);
+        case 4: return launch_dq<4>(a, s);
+        case 8: return launch_dq<8>(a, s);
+        case 16: return launch_dq<16>(a, s);
+        case 32: return launch_dq<32>(a, s);
+        case 64: return launch_dq<64>(a, s);
+        case 128: return launch_dq<128>(a, s);
+        case 256: return launch_dq<256>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace coat

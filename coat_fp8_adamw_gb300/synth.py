@@ -240,12 +240,21 @@ def grad_torch(wl: Workload, step: int, device, out=None) -> "torch.Tensor":
 
 
 def random_state_torch(n: int, G: int, seed: int, device):
-    """Device version of :func:`random_state_np` (same distributions, torch RNG)."""
+    """Device version of :func:`random_state_np` (same distributions, torch RNG).
+
+    Codes are drawn in chunks so that no full-size int32 temporary exists.
+    """
     gen = _gen(device, seed * 7919 + 3)
     ng = (n + G - 1) // G
-    r = torch.randint(0, 254, (n,), generator=gen, device=device, dtype=torch.int32)
-    mq = torch.where(r < 127, r, r + 1).to(torch.uint8)
-    vq = torch.randint(0, 127, (n,), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+    mq = torch.empty(n, dtype=torch.uint8, device=device)
+    vq = torch.empty(n, dtype=torch.uint8, device=device)
+    chunk = 1 << 28
+    for a in range(0, n, chunk):
+        b = min(n, a + chunk)
+        r = torch.randint(0, 254, (b - a,), generator=gen, device=device, dtype=torch.int32)
+        mq[a:b] = torch.where(r < 127, r, r + 1).to(torch.uint8)
+        r = torch.randint(0, 127, (b - a,), generator=gen, device=device, dtype=torch.int32)
+        vq[a:b] = r.to(torch.uint8)
     meta = torch.empty(ng, 4, dtype=torch.float32, device=device)
     meta[:, 0] = torch.exp2(torch.empty(ng, device=device).uniform_(-90.0, -20.0, generator=gen))
     meta[:, 1] = torch.empty(ng, device=device).uniform_(1.0, 8.0, generator=gen)

@@ -1,0 +1,127 @@
+/*
+ * coat.h -- C ABI of libcoat_gb300: the fused FP8 AdamW step with Dynamic
+ * Range Expansion (DRE), and the standalone DRE quantizer / dequantizer, for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method is COAT's ("COAT: Compressing Optimizer States and Activation
+ * for Memory-Efficient FP8 Training", paper-review page on the xllm-io blog):
+ *   - FP8 quantization (section 3, core formulas, "FP8量化"):
+ *       X_FP8 = round(X / S),  S = max|X| / 448         (448 = E4M3 max finite)
+ *   - AdamW (section 3, core formulas, "AdamW优化器更新规则"):
+ *       m_t = b1 m_{t-1} + (1-b1) g_t,   v_t = b2 v_{t-1} + (1-b2) g_t^2
+ *       mhat = m_t / (1-b1^t),           vhat = v_t / (1-b2^t)
+ *       w_{t+1} = w_t - lr (mhat / (sqrt(vhat) + eps) + wd w_t)
+ *   - Dynamic Range Expansion (section 3, "动态范围扩展"):
+ *       f(x) = sign(x)|x|^k,  R_X = max|X| / min|X|,  k = log_{R_X}(R_E4M3)
+ *   - the fused optimizer kernel (section 4 table, "融合优化器内核" row) and
+ *     per-shard statistics with no cross-GPU sync (section 4 table, FSDP row).
+ *
+ * Quantized state layout (all buffers flat, owned by the caller):
+ *   a tensor of n values is split into groups of G contiguous elements
+ *   (the last group may be shorter).  Each value is one E4M3 byte; each group
+ *   has a scale S and an exponent k.  A code q stands for
+ *       x = sign(q) * (|E4M3(q)| * S)^(1/k).
+ *   Quantization picks, per group, k = min(log(R_E4M3)/log(R_X), 8) with
+ *   min|X| taken over the non-zero elements, lowers k further if needed so
+ *   that S stays a normal float in [2^-125, 2^126], rounds k to float, sets
+ *   S = max|X|^k / 448 and encodes y = 448 sign(x) (|x|/max|X|)^k with
+ *   round-to-nearest-even onto the E4M3 grid, saturating at +-448 (0x7E /
+ *   0xFE); zero encodes as 0x00.  An all-zero group has S = 0, k = 1; a group
+ *   with one non-zero magnitude has k = 1.  R_E4M3 = 448 / 2^-9 = 229376
+ *   (see coat_r_e4m3()).
+ *
+ * Conventions for every entry point below:
+ *   - All data pointers are DEVICE pointers (cudaMalloc / torch CUDA tensors)
+ *     on the current device, 16-byte aligned.  The library allocates nothing
+ *     and keeps no state between calls.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is asynchronous on that stream.
+ *   - G must be a power of two in [1, 256]; n >= 1.
+ *   - Argument errors return a status and launch nothing.  A failed launch
+ *     returns COAT_ERR_CUDA (the CUDA error is left for the caller to query
+ *     with cudaGetLastError()).  Nothing aborts, traps or prints.
+ *   - Inputs must be finite; NaN/Inf inputs and the E4M3 NaN codes (0x7F,
+ *     0xFF) are outside the contract.
+ */
+#ifndef COAT_H_
+#define COAT_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    COAT_OK = 0,
+    COAT_ERR_INVALID_ARG = 1,   /* null pointer, n < 1, step < 1, bad hyper-parameter, aliasing */
+    COAT_ERR_MISALIGNED = 2,    /* a pointer is not 16-byte aligned */
+    COAT_ERR_UNSUPPORTED_G = 3, /* G not a power of two in [1, 256] */
+    COAT_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    COAT_ERR_NOT_DEVICE = 5     /* a pointer is not device (or managed) memory */
+} coat_status;
+
+/* Per-group record of the quantized optimizer state: 16 bytes, one per group,
+ * scale and exponent of the first moment, then of the second moment. */
+typedef struct {
+    float m_scale;
+    float m_k;
+    float v_scale;
+    float v_k;
+} coat_group_meta;
+
+/*
+ * One fused AdamW + DRE step over a flat parameter buffer, in one pass over
+ * HBM (COAT review page, section 3 core formulas and section 4 "fused
+ * optimizer kernel").  For every group of G elements it dequantizes m and v,
+ * undoes the expansion, applies the AdamW update above to w from the bf16
+ * gradient g, recomputes the group's k and S for both moments from the new
+ * fp32 moments and re-quantizes them.
+ *
+ *   w       [n] float32, in/out: master weights, updated in place.
+ *   g       [n] bfloat16 (raw 16-bit patterns), in: gradient of this step.
+ *   m_q,v_q [n] uint8, in/out: E4M3 codes of the first / second moment.
+ *   meta    [ceil(n/G)] coat_group_meta, in/out.
+ *   n, G    element count and group size.
+ *   beta1, beta2 in [0,1); lr >= 0; eps > 0; weight_decay >= 0; all finite.
+ *   step    t >= 1, the index of this update (bias correction uses b^t).
+ *
+ * First use: m_q = v_q = 0 and meta = {0, 1, 0, 1} for every group.
+ * g must not overlap any output buffer.  The moments used in the weight
+ * update are the fp32 values before re-quantization.
+ */
+coat_status coat_fp8_adamw_step(float *w, const uint16_t *g, uint8_t *m_q, uint8_t *v_q,
+                                coat_group_meta *meta, int64_t n, int32_t G, float beta1,
+                                float beta2, float lr, float eps, float weight_decay,
+                                int64_t step, void *stream);
+
+/*
+ * DRE + E4M3 quantization of one fp32 tensor (COAT review page, section 3,
+ * FP8 quantization and Dynamic Range Expansion equations).
+ *   x [n] float32 in;  q [n] uint8 out;  scale, k [ceil(n/G)] float32 out.
+ * x must not overlap the outputs.
+ */
+coat_status coat_dre_quantize(const float *x, int64_t n, int32_t G, uint8_t *q, float *scale,
+                              float *k, void *stream);
+
+/*
+ * Inverse of coat_dre_quantize: x = sign(q) (|E4M3(q)| scale)^(1/k).
+ *   q [n] uint8 in;  scale, k [ceil(n/G)] float32 in (k > 0);  x [n] float32 out.
+ */
+coat_status coat_dre_dequantize(const uint8_t *q, const float *scale, const float *k, int64_t n,
+                                int32_t G, float *x, void *stream);
+
+/* Static description of a status code (never NULL). */
+const char *coat_status_string(coat_status status);
+
+/* The R_E4M3 the library uses: 448 / 2^-9 = 229376. */
+double coat_r_e4m3(void);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int32_t coat_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COAT_H_ */

@@ -61,7 +61,10 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        # COAT_ORACLE_LIB lets the oracle's own mutation test load a deliberately
+        # broken build of coat_oracle.c in a subprocess
+        override = os.environ.get("COAT_ORACLE_LIB")
+        lib = ctypes.CDLL(override if override else build())
         c_f32p = ctypes.POINTER(ctypes.c_float)
         c_f64p = ctypes.POINTER(ctypes.c_double)
         c_u8p = ctypes.POINTER(ctypes.c_uint8)

@@ -1,0 +1,83 @@
+"""The C-ABI library loads, exports every declared symbol, and validates
+arguments on the host (CPU only: no call here reaches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import coat_fp8_adamw_gb300 as coat
+from coat_fp8_adamw_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return coat.lib()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "coat.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(coat_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared_functions()
+    assert set(declared) == set(coat.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_constants(L):
+    assert coat.coat_r_e4m3() == 448.0 * 2 ** 9
+    assert coat.coat_version() >= 100
+    for s, name in coat.STATUS.items():
+        assert coat.coat_status_string(s)
+    assert coat.coat_status_string(99) == "unknown status"
+
+
+A = 1 << 20  # a 16-byte aligned fake address: validation must reject before any access
+
+
+def _step(L, w=A, g=A + 0x100000, mq=A + 0x200000, vq=A + 0x300000, meta=A + 0x400000, n=256,
+          G=128, b1=0.9, b2=0.95, lr=1e-4, eps=1e-8, wd=0.1, step=1):
+    return L.coat_fp8_adamw_step(w, g, mq, vq, meta, n, G, b1, b2, lr, eps, wd, step, None)
+
+
+def test_step_validation(L):
+    assert _step(L, w=0) == 1
+    assert _step(L, n=0) == 1
+    assert _step(L, step=0) == 1
+    for G in (0, 3, 96, 512, -4):
+        assert _step(L, G=G) == 3
+    assert _step(L, w=A + 4) == 2
+    assert _step(L, meta=A + 0x400008) == 2
+    assert _step(L, b1=1.0) == 1
+    assert _step(L, b2=-0.1) == 1
+    assert _step(L, lr=float("nan")) == 1
+    assert _step(L, eps=0.0) == 1
+    assert _step(L, wd=-1.0) == 1
+    assert _step(L, g=A + 16) == 1              # gradient overlaps the weights
+    assert _step(L, vq=A + 0x200000 + 128) == 1  # codes overlap
+    # a well-formed call on memory that is not device memory is refused
+    assert _step(L) == 5
+
+
+def test_codec_validation(L):
+    assert L.coat_dre_quantize(0, 16, 16, A, A + 4096, A + 8192, None) == 1
+    assert L.coat_dre_quantize(A, 16, 7, A + 4096, A + 8192, A + 12288, None) == 3
+    assert L.coat_dre_quantize(A + 8, 16, 16, A + 4096, A + 8192, A + 12288, None) == 2
+    assert L.coat_dre_quantize(A, 64, 16, A + 16, A + 8192, A + 12288, None) == 1
+    assert L.coat_dre_quantize(A, 64, 16, A + 4096, A + 8192, A + 12288, None) == 5
+    assert L.coat_dre_dequantize(A, A + 4096, A + 8192, 0, 16, A + 12288, None) == 1
+    assert L.coat_dre_dequantize(A, A + 4096, A + 8192, 64, 16, A + 12288, None) == 5
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(coat, "_lib", None)
+    monkeypatch.setattr(coat._build, "lib_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        coat.lib()
