@@ -56,6 +56,29 @@ def dist_env():
     return ws, rank, local
 
 
+def aggregate(total_ms: float, params_per_rank: int, steps: int, device=None):
+    """Whole-job rate of independent replicas: every rank updates its own
+    parameter set; the job takes as long as its slowest rank.
+
+    Returns (max_ms_over_ranks, params_per_second_over_all_ranks).  With one
+    process (or no process group) it is the local figure.
+    """
+    import torch
+    ws = 1
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        import torch.distributed as dist
+        ws = dist.get_world_size()
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        n = torch.tensor([float(params_per_rank)], dtype=torch.float64, device=device)
+        dist.all_reduce(n, op=dist.ReduceOp.SUM)
+        total_params = float(n.item())
+    else:
+        total_params = float(params_per_rank)
+    return total_ms, total_params * steps / (total_ms / 1e3)
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
@@ -275,14 +298,8 @@ def run_ours(args):
     clk = clocks.stop()
     total_ms = t_begin.elapsed_time(t_end)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-
+    total_ms, value = aggregate(total_ms, n, args.steps, device=dev)
     ms_per_step = total_ms / args.steps
-    value = ws * n * args.steps / (total_ms / 1e3)
     avg_launch = statistics.mean(launch_ms)
     bpp = coat.bytes_per_param(G)
     achieved = bpp * n / (avg_launch / 1e3) / 1e9
@@ -325,12 +342,12 @@ def run_ours(args):
 
 
 def e2e_leg(args, coat, synth, torch, dev, w, g, mq, vq, meta, n, G, ng, hp, t):
-    """Same step through the public API with the state and gradient in pinned
-    host memory: each step copies w, g, codes and meta to the device, runs the
-    C-ABI step, and copies w, codes and meta back.  The whole state is streamed
-    in chunks through two device staging sets so that copies in both
-    directions overlap the kernel."""
-    chunk = min(n, 1 << 28)  # params per chunk (multiple of 256)
+    """The same step through the library's host-buffer entry point: w, g,
+    codes and meta live in pinned host memory, and coat_fp8_adamw_step_host
+    streams them through a device workspace (chunks on three streams, copies in
+    both directions overlapping the kernel).  Every step moves the whole state
+    host->device and back; the call returns when the host holds the result."""
+    chunk = min(n, 1 << 27)
     try:
         hw = torch.empty(n, dtype=torch.float32, pin_memory=True)
         hg = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
@@ -344,38 +361,12 @@ def e2e_leg(args, coat, synth, torch, dev, w, g, mq, vq, meta, n, G, ng, hp, t):
     hmq.copy_(mq)
     hvq.copy_(vq)
     hmeta.copy_(meta)
-    cg = chunk // G
-    bufs = []
-    for _ in range(2):
-        bufs.append((torch.empty(chunk, dtype=torch.float32, device=dev),
-                     torch.empty(chunk, dtype=torch.bfloat16, device=dev),
-                     torch.empty(chunk, dtype=torch.uint8, device=dev),
-                     torch.empty(chunk, dtype=torch.uint8, device=dev),
-                     torch.empty(cg, 4, dtype=torch.float32, device=dev)))
-    streams = [torch.cuda.Stream(dev) for _ in range(2)]
+    ws = torch.empty(coat.coat_fp8_adamw_step_host_workspace_bytes(chunk, G), dtype=torch.uint8,
+                     device=dev)
 
     def one_step(step_t):
-        for ci, a in enumerate(range(0, n, chunk)):
-            b = min(n, a + chunk)
-            m = b - a
-            ga, gb = a // G, (b + G - 1) // G
-            s = streams[ci % 2]
-            dw, dg, dm, dv, dmeta = bufs[ci % 2]
-            with torch.cuda.stream(s):
-                dw[:m].copy_(hw[a:b], non_blocking=True)
-                dg[:m].copy_(hg[a:b], non_blocking=True)
-                dm[:m].copy_(hmq[a:b], non_blocking=True)
-                dv[:m].copy_(hvq[a:b], non_blocking=True)
-                dmeta[:gb - ga].copy_(hmeta[ga:gb], non_blocking=True)
-                coat.coat_fp8_adamw_step(dw[:m], dg[:m], dm[:m], dv[:m], dmeta[:gb - ga], G,
-                                         hp["beta1"], hp["beta2"], hp["lr"], hp["eps"],
-                                         hp["weight_decay"], step_t, stream=s)
-                hw[a:b].copy_(dw[:m], non_blocking=True)
-                hmq[a:b].copy_(dm[:m], non_blocking=True)
-                hvq[a:b].copy_(dv[:m], non_blocking=True)
-                hmeta[ga:gb].copy_(dmeta[:gb - ga], non_blocking=True)
-        for s in streams:
-            s.synchronize()
+        coat.coat_fp8_adamw_step_host(hw, hg, hmq, hvq, hmeta, G, hp["beta1"], hp["beta2"],
+                                      hp["lr"], hp["eps"], hp["weight_decay"], step_t, ws)
 
     one_step(t + 1)  # warm-up
     t0 = time.perf_counter()
@@ -386,8 +377,8 @@ def e2e_leg(args, coat, synth, torch, dev, w, g, mq, vq, meta, n, G, ng, hp, t):
     d2h = n * (4 + 1 + 1) + ng * 16
     return {"value": n * args.e2e_steps / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "chunk_params": chunk,
-            "note": "state and gradient in pinned host memory, streamed through the C-ABI "
-                    "step in chunks on two streams; host wall clock"}
+            "note": "coat_fp8_adamw_step_host on pinned host buffers (state offloaded to host "
+                    "memory), host wall clock per call"}
 
 
 def main():

@@ -18,7 +18,8 @@ from typing import Optional
 
 from . import _build
 
-__all__ = ["CoatError", "coat_fp8_adamw_step", "coat_dre_quantize", "coat_dre_dequantize",
+__all__ = ["CoatError", "coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
+           "coat_fp8_adamw_step_host_workspace_bytes", "coat_dre_quantize", "coat_dre_dequantize",
            "coat_status_string", "coat_r_e4m3", "coat_version", "lib", "lib_path",
            "num_groups", "bytes_per_param", "STATUS"]
 
@@ -26,7 +27,8 @@ STATUS = {0: "COAT_OK", 1: "COAT_ERR_INVALID_ARG", 2: "COAT_ERR_MISALIGNED",
           3: "COAT_ERR_UNSUPPORTED_G", 4: "COAT_ERR_CUDA", 5: "COAT_ERR_NOT_DEVICE"}
 
 #: symbols the shared library must export (one per declaration in include/coat.h)
-EXPORTS = ("coat_fp8_adamw_step", "coat_dre_quantize", "coat_dre_dequantize",
+EXPORTS = ("coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
+           "coat_fp8_adamw_step_host_workspace_bytes", "coat_dre_quantize", "coat_dre_dequantize",
            "coat_status_string", "coat_r_e4m3", "coat_version")
 
 _lock = threading.Lock()
@@ -60,6 +62,11 @@ def lib() -> ctypes.CDLL:
         L.coat_fp8_adamw_step.argtypes = [vp, vp, vp, vp, vp, i64, i32, f32, f32, f32, f32, f32,
                                           i64, vp]
         L.coat_fp8_adamw_step.restype = ctypes.c_int
+        L.coat_fp8_adamw_step_host.argtypes = [vp, vp, vp, vp, vp, i64, i32, f32, f32, f32, f32,
+                                               f32, i64, vp, ctypes.c_size_t, vp]
+        L.coat_fp8_adamw_step_host.restype = ctypes.c_int
+        L.coat_fp8_adamw_step_host_workspace_bytes.argtypes = [i64, i32]
+        L.coat_fp8_adamw_step_host_workspace_bytes.restype = ctypes.c_size_t
         L.coat_dre_quantize.argtypes = [vp, i64, i32, vp, vp, vp, vp]
         L.coat_dre_quantize.restype = ctypes.c_int
         L.coat_dre_dequantize.argtypes = [vp, vp, vp, i64, i32, vp, vp]
@@ -148,6 +155,43 @@ def coat_fp8_adamw_step(w, g, m_q, v_q, meta, G: int, beta1: float, beta2: float
                                    _stream_ptr(stream))
     if st != 0:
         raise CoatError(st, "coat_fp8_adamw_step")
+
+
+def coat_fp8_adamw_step_host_workspace_bytes(chunk_params: int, G: int) -> int:
+    return int(lib().coat_fp8_adamw_step_host_workspace_bytes(int(chunk_params), int(G)))
+
+
+def _check_host(t, dtype, numel: int, name: str):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.is_cuda:
+        raise TypeError(f"{name} must be a CPU tensor of dtype {dtype}")
+    if not t.is_contiguous() or t.numel() != numel:
+        raise ValueError(f"{name} must be contiguous with {numel} elements")
+    return t.data_ptr()
+
+
+def coat_fp8_adamw_step_host(w, g, m_q, v_q, meta, G: int, beta1: float, beta2: float, lr: float,
+                             eps: float, weight_decay: float, step: int, workspace,
+                             stream=None) -> None:
+    """The step on host (ideally pinned) CPU tensors, streamed through the
+    device tensor ``workspace`` (uint8, see coat_fp8_adamw_step_host_workspace_bytes).
+    Returns when the host tensors hold the result."""
+    import torch
+    n = w.numel()
+    pw = _check_host(w, torch.float32, n, "w")
+    pg = _check_host(g, torch.bfloat16, n, "g")
+    pm = _check_host(m_q, torch.uint8, n, "m_q")
+    pv = _check_host(v_q, torch.uint8, n, "v_q")
+    pmeta = _check_host(meta, torch.float32, 4 * num_groups(n, G), "meta")
+    if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    st = lib().coat_fp8_adamw_step_host(pw, pg, pm, pv, pmeta, n, int(G), float(beta1),
+                                        float(beta2), float(lr), float(eps), float(weight_decay),
+                                        int(step), workspace.data_ptr(),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream_ptr(stream))
+    if st != 0:
+        raise CoatError(st, "coat_fp8_adamw_step_host")
 
 
 def coat_dre_quantize(x, G: int, q, scale, k, stream=None) -> None:

@@ -33,14 +33,17 @@ coat_status from_cuda(cudaError_t e) { return e == cudaSuccess ? COAT_OK : COAT_
 
 int64_t num_groups(int64_t n, int32_t G) { return (n + G - 1) / G; }
 
+
 }  // namespace
 
-extern "C" {
+namespace coat {
 
-coat_status coat_fp8_adamw_step(float* w, const uint16_t* g, uint8_t* m_q, uint8_t* v_q,
-                                coat_group_meta* meta, int64_t n, int32_t G, float beta1,
-                                float beta2, float lr, float eps, float weight_decay,
-                                int64_t step, void* stream) {
+// Checks shared by the device- and host-buffer steps (everything but where the
+// buffers live), and the per-launch constants.
+coat_status check_step_args(const float* w, const uint16_t* g, const uint8_t* m_q,
+                            const uint8_t* v_q, const coat_group_meta* meta, int64_t n, int32_t G,
+                            float beta1, float beta2, float lr, float eps, float weight_decay,
+                            int64_t step) {
     if (!w || !g || !m_q || !v_q || !meta || n < 1 || step < 1) return COAT_ERR_INVALID_ARG;
     if (!pow2_group(G)) return COAT_ERR_UNSUPPORTED_G;
     if (!aligned16(w) || !aligned16(g) || !aligned16(m_q) || !aligned16(v_q) || !aligned16(meta))
@@ -57,22 +60,17 @@ coat_status coat_fp8_adamw_step(float* w, const uint16_t* g, uint8_t* m_q, uint8
         overlaps(w, 4 * nb, meta, 16 * ng) || overlaps(m_q, nb, v_q, nb) ||
         overlaps(m_q, nb, meta, 16 * ng) || overlaps(v_q, nb, meta, 16 * ng))
         return COAT_ERR_INVALID_ARG;
-    if (!is_device(w) || !is_device(g) || !is_device(m_q) || !is_device(v_q) || !is_device(meta))
-        return COAT_ERR_NOT_DEVICE;
+    return COAT_OK;
+}
 
-    // bias corrections 1 - beta^t, once per launch, in double
+// Bias corrections 1 - beta^t once per launch in double; the kernel gets
+// lr / (1 - beta1^t), 1 / (1 - beta2^t), 1 - beta and 1 - lr wd as floats.
+coat_status make_step_args(float beta1, float beta2, float lr, float eps, float weight_decay,
+                           int64_t step, StepArgs& a) {
     const double b1 = beta1, b2 = beta2;
     const double bc1 = 1.0 - std::pow(b1, (double)step);
     const double bc2 = 1.0 - std::pow(b2, (double)step);
-    if (!(bc1 > 0.0) || !(bc2 > 0.0)) return COAT_ERR_INVALID_ARG;  // beta == 0 is fine: bc = 1
-
-    coat::StepArgs a;
-    a.w = w;
-    a.g = g;
-    a.mq = m_q;
-    a.vq = v_q;
-    a.meta = reinterpret_cast<float4*>(meta);
-    a.n = n;
+    if (!(bc1 > 0.0) || !(bc2 > 0.0)) return COAT_ERR_INVALID_ARG;
     a.beta1 = beta1;
     a.beta2 = beta2;
     a.omb1 = (float)(1.0 - b1);
@@ -81,6 +79,31 @@ coat_status coat_fp8_adamw_step(float* w, const uint16_t* g, uint8_t* m_q, uint8
     a.c2 = (float)(1.0 / bc2);
     a.eps = eps;
     a.decay = (float)(1.0 - (double)lr * (double)weight_decay);
+    return COAT_OK;
+}
+
+}  // namespace coat
+
+extern "C" {
+
+coat_status coat_fp8_adamw_step(float* w, const uint16_t* g, uint8_t* m_q, uint8_t* v_q,
+                                coat_group_meta* meta, int64_t n, int32_t G, float beta1,
+                                float beta2, float lr, float eps, float weight_decay,
+                                int64_t step, void* stream) {
+    coat_status st = coat::check_step_args(w, g, m_q, v_q, meta, n, G, beta1, beta2, lr, eps,
+                                           weight_decay, step);
+    if (st != COAT_OK) return st;
+    if (!is_device(w) || !is_device(g) || !is_device(m_q) || !is_device(v_q) || !is_device(meta))
+        return COAT_ERR_NOT_DEVICE;
+    coat::StepArgs a;
+    st = coat::make_step_args(beta1, beta2, lr, eps, weight_decay, step, a);
+    if (st != COAT_OK) return st;
+    a.w = w;
+    a.g = g;
+    a.mq = m_q;
+    a.vq = v_q;
+    a.meta = reinterpret_cast<float4*>(meta);
+    a.n = n;
     return from_cuda(coat::launch_adamw_dre_step(a, G, static_cast<cudaStream_t>(stream)));
 }
 

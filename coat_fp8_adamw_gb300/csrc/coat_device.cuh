@@ -14,7 +14,9 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#define COAT_CONST __constant__
 #include "coat_tables.inc"
+#include "coat_df.cuh"
 
 namespace coat {
 
@@ -31,8 +33,30 @@ constexpr float kGuardLo = 8.8073549220576041f - 125.0f;
 constexpr float kGuardHi = 8.8073549220576041f + 126.0f;
 
 // ---------------------------------------------------------------------------
-// SFU approximations, as documented PTX instructions (no flush-to-zero)
+// SFU approximations, as documented PTX instructions.  The .ftz forms are one
+// SFU instruction each; they flush subnormal inputs and results to zero,
+// which only touches values below 2^-126 (documented at each use).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2_ftz(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_ftz(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float sqrt_ftz(float x) {
+    float y;
+    asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -169,6 +193,62 @@ __device__ __forceinline__ QuantParams quant_params(float mx, float mn) {
     return q;
 }
 
+// Shared-memory copy of the double-float tables (divergent indices: constant
+// memory would serialize them).
+struct SmemTables {
+    float log2c_hi[64], log2c_lo[64];
+    float exp2j_hi[33], exp2j_lo[33];
+};
+
+__device__ __forceinline__ void load_smem_tables(SmemTables& st, int tid, int nthreads) {
+    for (int i = tid; i < 64; i += nthreads) {
+        st.log2c_hi[i] = __uint_as_float(kLog2CenterHi[i]);
+        st.log2c_lo[i] = __uint_as_float(kLog2CenterLo[i]);
+    }
+    for (int i = tid; i < 33; i += nthreads) {
+        st.exp2j_hi[i] = __uint_as_float(kExp2FracHi[i]);
+        st.exp2j_lo[i] = __uint_as_float(kExp2FracLo[i]);
+    }
+}
+
+__device__ __forceinline__ df::Tables tables_of(const SmemTables& st) {
+    return df::Tables{st.log2c_hi, st.log2c_lo, st.exp2j_hi, st.exp2j_lo};
+}
+
+__device__ __forceinline__ df::F2 const_df(const unsigned int* p) {
+    return df::F2{__uint_as_float(p[0]), __uint_as_float(p[1])};
+}
+
+// Fresh per-group parameters with k rounded once to fp32 from a ~2^-44
+// accurate value (so it equals the correctly rounded k except within 2^-44
+// of a rounding tie) and S = 2^(k log2 max - log2 448) rounded once.
+__device__ __forceinline__ QuantParams quant_params_precise(float mx, float mn,
+                                                            const df::Tables& t) {
+    QuantParams q;
+    if (!(mx > 0.0f)) {
+        q.k = 1.0f;
+        q.S = 0.0f;
+        q.inv_mx = 0.0f;
+        return q;
+    }
+    const df::F2 Lmx = df::log2_df(mx, t);
+    float k = 1.0f;
+    if (mn < mx) {
+        const df::F2 Lmn = df::log2_df(mn, t);
+        const df::F2 D = df::add2(Lmx, df::neg2(Lmn));
+        k = fminf(df::div22_rn(const_df(kLog2RDf), D), kKCap);
+    }
+    if (Lmx.hi < 0.0f)
+        k = fminf(k, df::div22_rn(const_df(kGuardLoDf), Lmx));
+    else if (Lmx.hi > 0.0f)
+        k = fminf(k, df::div22_rn(const_df(kGuardHiDf), Lmx));
+    const df::F2 e = df::add2(df::mul21(Lmx, k), df::neg2(const_df(kLog2_448Df)));
+    q.k = k;
+    q.S = df::exp2_df(e, t);
+    q.inv_mx = __frcp_rn(mx);
+    return q;
+}
+
 // Dequantize one code: sign(q) * P * 2^(L(q) * rk).
 __device__ __forceinline__ float dequant_one(const float* s_log_tab, uint32_t code, float P,
                                              float rk) {
@@ -183,6 +263,11 @@ __device__ __forceinline__ float dequant_one(const float* s_log_tab, uint32_t co
 __device__ __forceinline__ float expand_scaled(float x, float r, float k) {
     const float y = ex2_approx(fmaf(k, lg2_approx(r), kLog2_448));
     return __fadd_rn(copysignf(y, x), 0.0f);
+}
+
+// Same for a non-negative value (the second moment): no sign to carry.
+__device__ __forceinline__ float expand_scaled_pos(float r, float k) {
+    return ex2_approx(fmaf(k, lg2_approx(r), kLog2_448));
 }
 
 // Smallest-non-zero tracking: fp32 magnitudes as unsigned bits minus one, so

@@ -39,6 +39,21 @@ struct DequantArgs {
 };
 
 cudaError_t launch_adamw_dre_step(const StepArgs& a, int G, cudaStream_t stream);
+
+}  // namespace coat
+
+#include "coat.h"
+
+namespace coat {
+
+// argument checks shared by the device-buffer and host-buffer steps (coat_abi.cu)
+coat_status check_step_args(const float* w, const uint16_t* g, const uint8_t* m_q,
+                            const uint8_t* v_q, const coat_group_meta* meta, int64_t n, int32_t G,
+                            float beta1, float beta2, float lr, float eps, float weight_decay,
+                            int64_t step);
+// per-launch constants of the step (everything but the buffers)
+coat_status make_step_args(float beta1, float beta2, float lr, float eps, float weight_decay,
+                           int64_t step, StepArgs& a);
 cudaError_t launch_dre_quantize(const QuantArgs& a, int G, cudaStream_t stream);
 cudaError_t launch_dre_dequantize(const DequantArgs& a, int G, cudaStream_t stream);
 

@@ -22,6 +22,10 @@ template <int G>
 __global__ void __launch_bounds__(kThreads)
 dre_quantize_kernel(const QuantArgs a) {
     using Gm = Geom<G>;
+    __shared__ SmemTables st;
+    load_smem_tables(st, threadIdx.x, kThreads);
+    __syncthreads();
+    const df::Tables tab = tables_of(st);
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t base = tid * kVec;
     if (__all_sync(0xFFFFFFFFu, base >= a.n)) return;
@@ -61,7 +65,7 @@ dre_quantize_kernel(const QuantArgs a) {
     float pre[Gm::kGroups];
 #pragma unroll
     for (int j = 0; j < Gm::kGroups; ++j) {
-        qp[j] = quant_params(mx[j], nz_key_value(mn[j]));
+        qp[j] = quant_params_precise(mx[j], nz_key_value(mn[j]), tab);
         pre[j] = 1.0f;
         if (mx[j] > 0.0f && mx[j] < 1.17549435e-38f) {
             pre[j] = 16777216.0f;

@@ -31,11 +31,16 @@
  *   (see coat_r_e4m3()).
  *
  * Conventions for every entry point below:
- *   - All data pointers are DEVICE pointers (cudaMalloc / torch CUDA tensors)
- *     on the current device, 16-byte aligned.  The library allocates nothing
- *     and keeps no state between calls.
+ *   - Data pointers are DEVICE pointers (cudaMalloc / torch CUDA tensors) on
+ *     the current device, 16-byte aligned -- except the state buffers of
+ *     coat_fp8_adamw_step_host, which are host pointers.  The library
+ *     allocates no memory and keeps no state between calls
+ *     (coat_fp8_adamw_step_host creates and destroys its three streams and
+ *     one event within the call).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
- *     stream).  Every call is asynchronous on that stream.
+ *     stream).  Every call is asynchronous on that stream, except
+ *     coat_fp8_adamw_step_host, which returns when its result is in host
+ *     memory.
  *   - G must be a power of two in [1, 256]; n >= 1.
  *   - Argument errors return a status and launch nothing.  A failed launch
  *     returns COAT_ERR_CUDA (the CUDA error is left for the caller to query
@@ -46,6 +51,7 @@
 #ifndef COAT_H_
 #define COAT_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -94,6 +100,31 @@ coat_status coat_fp8_adamw_step(float *w, const uint16_t *g, uint8_t *m_q, uint8
                                 coat_group_meta *meta, int64_t n, int32_t G, float beta1,
                                 float beta2, float lr, float eps, float weight_decay,
                                 int64_t step, void *stream);
+
+/*
+ * The same step with the optimizer state and the gradient in HOST memory
+ * (state offloading).  w, g, m_q, v_q and meta are host pointers, laid out as
+ * for coat_fp8_adamw_step; page-locked (pinned) memory lets the copies run
+ * asynchronously and overlap, pageable memory works but is slower.  The
+ * state is streamed through `workspace` (device memory owned by the caller,
+ * 256-byte aligned, `workspace_bytes` long) in chunks of equal size, a
+ * multiple of 4096 parameters: host->device copies, the kernel and
+ * device->host copies of consecutive chunks run on three internal streams
+ * that start after the work already queued on `stream`.  The call returns
+ * once the host buffers hold the updated state (or on error); the result is
+ * bit-identical to coat_fp8_adamw_step on device copies of the same buffers.
+ * COAT_ERR_INVALID_ARG also covers: a state buffer that is device memory, a
+ * workspace too small for one chunk (see coat_fp8_adamw_step_host_workspace_bytes).
+ */
+coat_status coat_fp8_adamw_step_host(float *w, const uint16_t *g, uint8_t *m_q, uint8_t *v_q,
+                                     coat_group_meta *meta, int64_t n, int32_t G, float beta1,
+                                     float beta2, float lr, float eps, float weight_decay,
+                                     int64_t step, void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
+/* Workspace bytes coat_fp8_adamw_step_host needs to stream chunks of
+ * `chunk_params` parameters (rounded up to a multiple of 4096); 0 for a bad G. */
+size_t coat_fp8_adamw_step_host_workspace_bytes(int64_t chunk_params, int32_t G);
 
 /*
  * DRE + E4M3 quantization of one fp32 tensor (COAT review page, section 3,

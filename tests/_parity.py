@@ -5,7 +5,10 @@ Tolerances (floating point, from the stated targets of this port):
   * E4M3 codes: at most 1e-4 of the codes differ, each by one step of the
     E4M3 grid (adjacent codes of the same sign, or 0x00 / +-0x01);
   * k: relative 1e-6;
-  * S: relative 1e-6 where the scale is well conditioned; see ``s_tolerance``.
+  * S: relative 1e-6.  S = max^k / 448 is ill-conditioned in the group's
+    extreme moments (condition number up to ~30), so this holds only because
+    the kernel re-evaluates those extremes exactly; ``s_condition`` gives the
+    sensitivity for diagnostics.
 """
 from __future__ import annotations
 
@@ -75,11 +78,31 @@ def compare_meta(gpu_S, gpu_k, ref_S, ref_k, what: str, state_rel: float = STATE
     assert np.array_equal(gS == 0, zero), f"{what}: zero scales differ"
     srel = np.zeros_like(rS)
     srel[~zero] = np.abs(gS[~zero] / rS[~zero] - 1.0)
-    ks, kk = s_condition(rS, rk)
-    bound = S_RTOL + ks * state_rel + kk * K_REL
-    bad = srel > bound
-    assert not bad.any(), (f"{what}: {int(bad.sum())} scales beyond the propagated bound; "
-                           f"worst rel {srel.max():.3e}")
+    bad = srel > S_RTOL
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {srel.size} scales differ by more than "
+                           f"{S_RTOL} relative; worst {srel.max():.3e}")
     return {"k_max_rel": float(krel.max()), "S_max_rel": float(srel.max()),
-            "S_frac_within_1e-6": float((srel <= S_RTOL).mean()),
-            "S_worst_over_bound": float((srel / bound).max())}
+            "k_bit_equal_frac": float((gk == rk).mean()),
+            "S_bit_equal_frac": float((gS == rS).mean())}
+
+
+def adamw_like_state(n: int, G: int, seed: int, oracle):
+    """A non-zero optimizer state coupled like real AdamW moments, quantized by the oracle.
+
+    Per group a gradient scale s is drawn log-uniform in [1e-6, 1e-2]; per
+    element s_e = s exp(0.5 z); then m ~ 0.23 s_e N(0, 1) (the spread of an
+    EMA with beta1 = 0.9 of i.i.d. gradients) and v ~ s_e^2 (0.5 + U[0, 1]).
+    Independent random codes would pair a large first moment with a tiny
+    second moment, an update no AdamW trajectory produces.
+    """
+    import numpy as np
+    rng = np.random.default_rng([seed, 31])
+    ng = (n + G - 1) // G
+    s = np.repeat(10.0 ** rng.uniform(-6, -2, ng), G)[:n]
+    se = s * np.exp(0.5 * rng.standard_normal(n))
+    m = (0.23 * se * rng.standard_normal(n)).astype(np.float32)
+    v = (se * se * (0.5 + rng.random(n))).astype(np.float32)
+    mq, Sm, km = oracle.dre_quantize(m, G)
+    vq, Sv, kv = oracle.dre_quantize(v, G)
+    meta = np.stack([Sm, km, Sv, kv], axis=1).astype(np.float32)
+    return mq, vq, np.ascontiguousarray(meta)

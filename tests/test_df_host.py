@@ -1,0 +1,34 @@
+"""Host-side check of the kernels' double-float toolkit (CPU only).
+
+coat_df.cuh is built only from IEEE add / multiply / fma / divide, so the
+same code compiled for the host gives the results the device gets.  The
+harness in tests/native/df_check.cpp compares it with float64 libm.
+"""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_double_float_toolkit_accuracy(tmp_path):
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    exe = tmp_path / "df_check"
+    subprocess.run([cxx, "-O2", "-std=c++17", "-ffp-contract=off",
+                    "-I", os.path.join(ROOT, "coat_fp8_adamw_gb300", "csrc"),
+                    os.path.join(ROOT, "tests", "native", "df_check.cpp"), "-o", str(exe), "-lm"],
+                   check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout
+    stats = dict(kv.split("=") for kv in out.split())
+    stats = {k: float(v) for k, v in stats.items()}
+    print(stats)
+    assert stats["log2_max_abs"] < 2.0 ** -40          # |log2 x| <= 149: ~2^-48 relative
+    assert stats["log2_max_abs_near1"] < 2.0 ** -44
+    assert stats["exp2_miss_frac"] < 1e-5              # correctly rounded except near ties
+    assert stats["exp2_max_rel"] <= 2.0 ** -24 * 1.0001
+    assert stats["div_miss_frac"] < 1e-5
+    assert stats["dot_miss_frac"] < 1e-5

@@ -79,12 +79,12 @@ def test_tiny_trajectory_teacher_forced():
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 16, 32, 64, 128, 256])
-def test_random_state_every_group_size(G):
+def test_adamw_like_state_every_group_size(G):
     n = 4096 * 3 + 77                       # several CTAs and a ragged tail
     rng = np.random.default_rng(G)
     w = (rng.standard_normal(n) * 0.02).astype(np.float32)
     g = synth.f32_to_bf16_bits((rng.standard_normal(n) * 10.0 ** rng.uniform(-5, -2, n)).astype(np.float32))
-    mq, vq, meta = synth.random_state_np(n, G, seed=100 + G)
+    mq, vq, meta = P.adamw_like_state(n, G, 100 + G, oracle)
     ref = oracle_step(w, g, mq, vq, meta, G, 7)
     gpu = gpu_step(w, g, mq, vq, meta, G, 7)
     check(gpu, ref, f"random G={G}")
@@ -96,7 +96,7 @@ def test_small_and_ragged_sizes(n):
     rng = np.random.default_rng(n)
     w = (rng.standard_normal(n) * 0.02).astype(np.float32)
     g = synth.f32_to_bf16_bits((rng.standard_normal(n) * 1e-3).astype(np.float32))
-    mq, vq, meta = synth.random_state_np(n, G, seed=n)
+    mq, vq, meta = P.adamw_like_state(n, G, n, oracle)
     check(gpu_step(w, g, mq, vq, meta, G, 2), oracle_step(w, g, mq, vq, meta, G, 2), f"n={n}")
 
 
@@ -151,7 +151,7 @@ def test_large_step_count_and_hyperparameters():
     rng = np.random.default_rng(11)
     w = (rng.standard_normal(n) * 0.02).astype(np.float32)
     g = synth.f32_to_bf16_bits((rng.standard_normal(n) * 1e-3).astype(np.float32))
-    mq, vq, meta = synth.random_state_np(n, G, seed=9)
+    mq, vq, meta = P.adamw_like_state(n, G, 9, oracle)
     for hp, step in ((dict(HP), 1_000_000), (dict(beta1=0.5, beta2=0.999, lr=3e-3, eps=1e-6,
                                                    weight_decay=0.0), 3)):
         check(gpu_step(w, g, mq, vq, meta, G, step, hp), oracle_step(w, g, mq, vq, meta, G, step, hp),
@@ -164,7 +164,7 @@ def test_in_place_and_stream_semantics():
     rng = np.random.default_rng(12)
     w = (rng.standard_normal(n) * 0.02).astype(np.float32)
     g = synth.f32_to_bf16_bits((rng.standard_normal(n) * 1e-3).astype(np.float32))
-    mq, vq, meta = synth.random_state_np(n, G, seed=12)
+    mq, vq, meta = P.adamw_like_state(n, G, 12, oracle)
     a = gpu_step(w, g, mq, vq, meta, G, 4)
     s = torch.cuda.Stream()
     w_d, g_d = _dev(w.copy()), _dev(g.view(np.int16), torch.bfloat16)
