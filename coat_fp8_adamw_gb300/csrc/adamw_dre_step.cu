@@ -19,20 +19,28 @@
 // moments: k ~ 4, log2 max ~ -25), and the smallest |m_t| of a group usually
 // comes from a partial cancellation of beta1 m and (1 - beta1) g, where an
 // fp32 evaluation has a large relative error.  So every element's moment is
-// first computed on a fast fp32/SFU path whose error is bounded (kFastErr);
-// the elements whose fast value lies within twice that bound of the group's
-// fast max (min) are re-evaluated exactly -- (|E4M3(q)| S)^(1/k) in
-// double-float, rounded once, then beta x + (1 - beta) g as a correctly
-// rounded sum of two products -- and the group's max and min are taken over
-// those exact values.  k and S are formed from them in double-float and
-// rounded once.  All codes are encoded from the fast values and the exact
-// (max, k).
+// first computed on a fast fp32/SFU path whose error has a per-group bound;
+// the elements whose fast value lies inside that bound around the group's
+// fast max or min -- and the first moments so small that cancellation could
+// move their code by more than one step -- are re-evaluated exactly:
+// (|E4M3(q)| S)^(1/k) in double-float rounded once (a plain product when
+// k = 1), then beta x + (1 - beta) g as a correctly rounded sum of two
+// products.  The group's max and min are taken over those exact values, k and
+// S are formed from them in double-float and rounded once, and the
+// re-evaluated elements are encoded from their exact values.
 //
-// Layout: every thread owns 16 consecutive parameters, so each stream is
-// whole 128-bit accesses: w 4x16 B, g 2x16 B, m codes 16 B, v codes 16 B;
-// the 16-byte (S_m, k_m, S_v, k_v) record per group is one 128-bit access.
-// For G >= 32 a group spans G/16 adjacent lanes of a warp and the per-group
-// work is split across them; for G <= 16 a thread holds 16/G whole groups.
+// Execution.  A CTA of 256 threads owns 4096 consecutive parameters (16 per
+// thread: every stream is whole 128-bit accesses).  The per-group work runs
+// as CTA-wide jobs between barriers -- one thread per (group, moment) or per
+// (group, statistic) -- so that it occupies a few full warps instead of a few
+// lanes of every warp; the moments wait in shared memory between phases.
+//   B  stored-state parameters            2 jobs per group
+//   C  fast path, statistics, candidates   every thread
+//   D1 candidate masks                     4 jobs per group
+//   D2 exact re-evaluation                 4 jobs per group
+//   E  k, S, encoding constants, record    2 jobs per group
+//   F  encode and store codes              every thread
+// Groups of G < 16 parameters live inside one thread (step_kernel_thread).
 #include <cstddef>
 
 #include "coat_device.cuh"
@@ -44,46 +52,21 @@ namespace {
 
 using df::F2;
 
-constexpr int kStepThreads = 128;   // 4 warps per CTA
 constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kCta = 256;                  // threads per CTA
+constexpr int kCtaElems = kCta * kVec;     // parameters per CTA
+#define kInf __int_as_float(0x7F800000)
 
-// Bound on the relative error of a fast dequantized moment (SFU exp2 2^-22,
-// the fp32 exponent L(q)/k with |L(q)/k| <= 277 rounded three times, P a few
-// ulp, two roundings) with ample margin.  Through the EMA it bounds the error
-// of v_t relative to v_t and of m_t relative to |beta1 m| + |(1-beta1) g|.
-constexpr float kFastErr = 6.103515625e-05f;   // 2^-14
+// Relative error bound of the SFU exp2 (ex2.approx.ftz.f32), with margin.
+constexpr float kEx2Err = 4.76837158203125e-07f;   // 2^-21
 
-template <int G>
-struct Geom {
-    static constexpr int kLanes = G >= kVec ? G / kVec : 1;   // lanes per group
-    static constexpr int kGroups = G >= kVec ? 1 : kVec / G;  // groups per thread
-    static constexpr int kElems = G >= kVec ? kVec : G;       // elements per (thread, group)
-};
-
-// Per-warp staging: the fast moments and the raw inputs of every lane, read
-// by the lanes that look for and re-evaluate a group's extreme elements.
-// Row strides (20 and 12 words) keep the 128-bit stores bank-conflict free;
-// every row starts on a 16-byte boundary (128-bit shared-memory stores).
-struct alignas(16) WarpStage {
-    float m[32][20];
-    float v[32][20];
-    uint32_t mq[32][4];
-    uint32_t vq[32][4];
-    uint32_t g[32][12];
-};
-
-struct StepSmem {
-    WarpStage stage[kStepThreads / 32];   // first: 16-byte aligned at offset 0
-    float lg_hi[128];
-    float lg_lo[128];
-    SmemTables t;
-};
-static_assert(offsetof(StepSmem, stage) % 16 == 0, "staging must be 16-byte aligned");
-static_assert(sizeof(WarpStage) % 16 == 0, "per-warp staging must keep 16-byte alignment");
-static_assert(offsetof(WarpStage, m) % 16 == 0 && offsetof(WarpStage, v) % 16 == 0 &&
-              offsetof(WarpStage, mq) % 16 == 0 && offsetof(WarpStage, vq) % 16 == 0 &&
-              offsetof(WarpStage, g) % 16 == 0, "rows of 128-bit stores");
-static_assert((20 * 4) % 16 == 0 && (12 * 4) % 16 == 0 && (4 * 4) % 16 == 0, "row strides");
+// Bound on the relative error of a fast dequantized moment of a group whose
+// stored exponent is k (1/k = rk): the SFU exp2 of the factor P and of the
+// per-code term, the fp32 exponent log2(|E4M3(q)|/448) / k (|.| <= 17.81/k)
+// rounded three times, and two roundings.
+__device__ __forceinline__ float fast_err(float rk) {
+    return 2.0f * kEx2Err + 1.5e-7f + 1.25e-07f * (17.81f * rk + 1.0f);
+}
 
 struct Chunk {
     float w[kVec];
@@ -138,6 +121,19 @@ __device__ __forceinline__ void zero_chunk(Chunk& c) {
     for (int i = 0; i < kVec / 4; ++i) { c.mq[i] = 0u; c.vq[i] = 0u; }
 }
 
+__device__ __forceinline__ void store_w(const StepArgs& a, int64_t base, bool full, const Chunk& c) {
+    if (full) {
+        float4* wp = reinterpret_cast<float4*>(a.w + base);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            st_cs(wp + i, make_float4(c.w[4 * i], c.w[4 * i + 1], c.w[4 * i + 2], c.w[4 * i + 3]));
+    } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e)
+            if (base + e < a.n) a.w[base + e] = c.w[e];
+    }
+}
+
 __device__ __forceinline__ uint32_t byte_of(const uint32_t* w, int j) {
     return (w[j >> 2] >> (8 * (j & 3))) & 0xFFu;
 }
@@ -145,16 +141,24 @@ __device__ __forceinline__ float bf16_of(const uint32_t* w, int j) {
     return (j & 1) ? __uint_as_float(w[j >> 1] & 0xFFFF0000u) : __uint_as_float(w[j >> 1] << 16);
 }
 
+// Value of a non-negative E4M3 magnitude code (bias 7, subnormal below 8).
+__device__ __forceinline__ float e4m3_value(uint32_t mag) {
+    return mag >= 8u ? __uint_as_float((((mag >> 3) + 120u) << 23) | ((mag & 7u) << 20))
+                     : __fmul_rn((float)mag, 0.001953125f);
+}
+
 // Parameters of one stored moment.  Exact path: A = log2(448 S) and 1/k as
-// double-floats.  Fast path: P = (448 S)^(1/k) and 1/k as floats.
+// double-floats (and S itself for k = 1).  Fast path: P = (448 S)^(1/k), 1/k.
 struct StateParams {
     F2 A;
     F2 rkd;
     float P;
+    float S;
 };
 
 __device__ __forceinline__ StateParams state_params(float S, float k, const df::Tables& t) {
     StateParams p;
+    p.S = S;
     p.rkd = df::div21(F2{1.0f, 0.0f}, k);
     if (S > 0.0f) {
         p.A = df::add2(df::log2_df(S, t), const_df(kLog2_448Df));
@@ -171,15 +175,21 @@ __device__ __forceinline__ StateParams state_params(float S, float k, const df::
 // Exactly rounded new moment of one element:
 //   prev = sign(q) RN((|E4M3(q)| S)^(1/k)),  RN(beta prev + (1-beta) x),
 // with x = g (first moment) or g^2 (second moment, exact for a bf16 g).
-__device__ __forceinline__ float exact_moment(uint32_t code, float gf, bool second,
-                                              const StateParams& sp, float beta, float omb,
+// For k = 1 the power is the plain product |E4M3(q)| S, which is often a
+// rounding tie: it is formed by one correctly rounded multiplication.
+__device__ __forceinline__ float exact_moment(uint32_t code, float gf, bool second, F2 A, F2 rkd,
+                                              float S, float beta, float omb,
                                               const df::Tables& t, const float* lg_hi,
                                               const float* lg_lo) {
     float prev = 0.0f;
     const uint32_t mag = code & 0x7Fu;
-    if (mag != 0u && sp.P > 0.0f) {
-        const F2 L = {lg_hi[mag], lg_lo[mag]};
-        prev = df::exp2_df(df::mul22(df::add2(L, sp.A), sp.rkd), t);
+    if (mag != 0u && S > 0.0f) {
+        if (rkd.hi == 1.0f && rkd.lo == 0.0f) {
+            prev = __fmul_rn(e4m3_value(mag), S);
+        } else {
+            const F2 L = {lg_hi[mag], lg_lo[mag]};
+            prev = df::exp2_df(df::mul22(df::add2(L, A), rkd), t);
+        }
         if (code & 0x80u) prev = -prev;
     }
     const float x = second ? __fmul_rn(gf, gf) : gf;
@@ -188,8 +198,29 @@ __device__ __forceinline__ float exact_moment(uint32_t code, float gf, bool seco
 
 // k rounded once from double-float logs of the group's max / min magnitudes,
 // with the cap and the S-range guard; S = 2^(k log2 max - log2 448) rounded once.
-__device__ __forceinline__ void k_and_S(float mx, float mn, F2 Lmx, F2 Lmn, const df::Tables& t,
-                                        float& k, float& S) {
+__device__ __forceinline__ void k_and_S(float mx, float mn, const df::Tables& t, float& k,
+                                        float& S) {
+    if (!(mx > 0.0f)) {
+        k = 1.0f;
+        S = 0.0f;
+        return;
+    }
+    const F2 Lmx = df::log2_df(mx, t);
+    k = 1.0f;
+    if (mn > 0.0f && mn < mx) {
+        const F2 Lmn = df::log2_df(mn, t);
+        k = fminf(df::div22_rn(const_df(kLog2RDf), df::add2(Lmx, df::neg2(Lmn))), kKCap);
+    }
+    if (Lmx.hi < 0.0f)
+        k = fminf(k, df::div22_rn(const_df(kGuardLoDf), Lmx));
+    else if (Lmx.hi > 0.0f)
+        k = fminf(k, df::div22_rn(const_df(kGuardHiDf), Lmx));
+    S = df::exp2_df(df::add2(df::mul21(Lmx, k), df::neg2(const_df(kLog2_448Df))), t);
+}
+
+// The same from logs computed elsewhere (Lmx, Lmn: log2 of mx, mn).
+__device__ __forceinline__ void k_and_S_logs(float mx, float mn, F2 Lmx, F2 Lmn,
+                                             const df::Tables& t, float& k, float& S) {
     if (!(mx > 0.0f)) {
         k = 1.0f;
         S = 0.0f;
@@ -205,22 +236,12 @@ __device__ __forceinline__ void k_and_S(float mx, float mn, F2 Lmx, F2 Lmn, cons
     S = df::exp2_df(df::add2(df::mul21(Lmx, k), df::neg2(const_df(kLog2_448Df))), t);
 }
 
-// Encoding constants of one group: r = |x| * inv, z = k log2 r + cz.  A
-// subnormal max is pre-scaled by 2^24 (inv = 1/(max 2^24)) and the factor is
-// folded back into cz.
-struct EncodeParams {
-    float inv;
-    float k;
-    float cz;
-};
-
-__device__ __forceinline__ EncodeParams encode_params(float mx, float k) {
-    EncodeParams e;
-    e.k = k;
+// Encoding constants: r = |x| * inv, y = 2^(k log2 r + cz).  A subnormal max
+// is pre-scaled by 2^24 (inv = 1/(max 2^24)) and the factor folded into cz.
+__device__ __forceinline__ void encode_consts(float mx, float k, float& inv, float& cz) {
     const bool sub = mx < 1.17549435e-38f;
-    e.inv = mx > 0.0f ? __frcp_rn(sub ? mx * 16777216.0f : mx) : 0.0f;
-    e.cz = sub ? fmaf(24.0f, k, kLog2_448) : kLog2_448;
-    return e;
+    inv = mx > 0.0f ? __frcp_rn(sub ? mx * 16777216.0f : mx) : 0.0f;
+    cz = sub ? fmaf(24.0f, k, kLog2_448) : kLog2_448;
 }
 
 // Smallest-non-zero keys: 2 * bits(|x|) - 2 as unsigned drops the sign and
@@ -230,356 +251,480 @@ __device__ __forceinline__ float min_key_value(uint32_t k) {
     return k >= 0xFFFFFFFEu ? 0.0f : __uint_as_float((k + 2u) >> 1);
 }
 
-// ---------------------------------------------------------------------------
-// the fast path over one thread's 16 elements (shared by both kernels)
-// ---------------------------------------------------------------------------
-template <int NG, int E>
-__device__ __forceinline__ void fast_path(const StepArgs& a, Chunk& c, const float* lg,
-                                          const float* Pm, const float* rkm, const float* Pv,
-                                          const float* rkv, float* m, float* v, float* mx_m,
-                                          uint32_t* mn_m, float* mx_v, uint32_t* mn_v,
-                                          float* mx_g) {
-#pragma unroll
-    for (int j = 0; j < NG; ++j) {
-        mx_m[j] = 0.0f; mx_v[j] = 0.0f; mx_g[j] = 0.0f; mn_m[j] = 0xFFFFFFFEu; mn_v[j] = 0xFFFFFFFEu;
-    }
-#pragma unroll
-    for (int e = 0; e < kVec; ++e) {
-        const int j = e / E;
-        const uint32_t wm = c.mq[e / 4] >> (8 * (e & 3));
-        const uint32_t wv = c.vq[e / 4] >> (8 * (e & 3));
-        // dequantize: |x| = P 2^(L(q)/k); the code's sign goes onto P, and the
-        // "+ 0" keeps a zero magnitude at +0 whatever the sign bit
-        const float em = ex2_ftz(__fmul_rn(lg[wm & 0x7Fu], rkm[j]));
-        const float Ps = __uint_as_float(__float_as_uint(Pm[j]) | ((wm & 0x80u) << 24));
-        const float m_prev = fmaf(em, Ps, 0.0f);
-        const float v_prev = __fmul_rn(Pv[j], ex2_ftz(__fmul_rn(lg[wv & 0x7Fu], rkv[j])));
-        const float gf = bf16_of(c.g, e);
-        const float mt = fmaf(a.beta1, m_prev, __fmul_rn(a.omb1, gf));
-        const float vt = fmaf(a.beta2, v_prev, __fmul_rn(__fmul_rn(a.omb2, gf), gf));
-        // AdamW; sqrt/rcp on the SFU (flush-to-zero only below 2^-126)
-        const float denom = __fadd_rn(sqrt_ftz(__fmul_rn(vt, a.c2)), a.eps);
-        c.w[e] = fmaf(__fmul_rn(-a.c1, mt), rcp_ftz(denom), __fmul_rn(c.w[e], a.decay));
-        m[e] = mt;
-        v[e] = vt;
-        mx_m[j] = fmaxf(mx_m[j], fabsf(mt));
-        mx_v[j] = fmaxf(mx_v[j], vt);
-        mx_g[j] = fmaxf(mx_g[j], fabsf(gf));
-        mn_m[j] = min(mn_m[j], min_key(mt));
-        mn_v[j] = min(mn_v[j], min_key(vt));
-    }
+// Fast path of one element: dequantize, EMAs, AdamW.  The code's sign goes
+// onto P, and the "+ 0" keeps a zero magnitude at +0 whatever the sign bit;
+// SFU ops flush below 2^-126 only.
+__device__ __forceinline__ void fast_elem(const StepArgs& a, uint32_t wm, uint32_t wv, float gf,
+                                          float& w, const float* lg, float Pm, float rkm,
+                                          float Pv, float rkv, float& mt, float& vt) {
+    const float em = ex2_ftz(__fmul_rn(lg[wm & 0x7Fu], rkm));
+    const float Ps = __uint_as_float(__float_as_uint(Pm) | ((wm & 0x80u) << 24));
+    const float m_prev = fmaf(em, Ps, 0.0f);
+    const float v_prev = __fmul_rn(Pv, ex2_ftz(__fmul_rn(lg[wv & 0x7Fu], rkv)));
+    mt = fmaf(a.beta1, m_prev, __fmul_rn(a.omb1, gf));
+    vt = fmaf(a.beta2, v_prev, __fmul_rn(__fmul_rn(a.omb2, gf), gf));
+    const float denom = __fadd_rn(sqrt_ftz(__fmul_rn(vt, a.c2)), a.eps);
+    w = fmaf(__fmul_rn(-a.c1, mt), rcp_ftz(denom), __fmul_rn(w, a.decay));
 }
 
-// Encode 16 moments and store weights, codes.
-template <int NG, int E>
-__device__ __forceinline__ void encode_store(const StepArgs& a, int64_t base, bool full,
-                                             const Chunk& c, const float* m, const float* v,
-                                             const EncodeParams* em, const EncodeParams* ev) {
-    uint32_t om[kVec / 4], ov[kVec / 4];
-#pragma unroll
-    for (int e = 0; e < kVec; e += 2) {
-        const int j0 = e / E, j1 = (e + 1) / E;
-        const float ym0 = copysignf(ex2_ftz(fmaf(em[j0].k, lg2_ftz(fabsf(m[e]) * em[j0].inv), em[j0].cz)), m[e]);
-        const float ym1 = copysignf(ex2_ftz(fmaf(em[j1].k, lg2_ftz(fabsf(m[e + 1]) * em[j1].inv), em[j1].cz)), m[e + 1]);
-        const float yv0 = ex2_ftz(fmaf(ev[j0].k, lg2_ftz(v[e] * ev[j0].inv), ev[j0].cz));
-        const float yv1 = ex2_ftz(fmaf(ev[j1].k, lg2_ftz(v[e + 1] * ev[j1].inv), ev[j1].cz));
-        const uint32_t pm = e4m3x2(ym0, ym1);
-        const uint32_t pv = e4m3x2(yv0, yv1);
-        if ((e & 2) == 0) { om[e / 4] = pm; ov[e / 4] = pv; }
-        else { om[e / 4] |= pm << 16; ov[e / 4] |= pv << 16; }
-    }
-    if (full) {
-        float4* wp = reinterpret_cast<float4*>(a.w + base);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            st_cs(wp + i, make_float4(c.w[4 * i], c.w[4 * i + 1], c.w[4 * i + 2], c.w[4 * i + 3]));
-        st_cs(reinterpret_cast<uint4*>(a.mq + base), make_uint4(om[0], om[1], om[2], om[3]));
-        st_cs(reinterpret_cast<uint4*>(a.vq + base), make_uint4(ov[0], ov[1], ov[2], ov[3]));
-    } else {
-#pragma unroll
-        for (int e = 0; e < kVec; ++e) {
-            if (base + e < a.n) {
-                a.w[base + e] = c.w[e];
-                a.mq[base + e] = (uint8_t)(om[e / 4] >> (8 * (e & 3)));
-                a.vq[base + e] = (uint8_t)(ov[e / 4] >> (8 * (e & 3)));
-            }
-        }
-    }
+__device__ __forceinline__ uint32_t encode_pair_m(float m0, float m1, float k, float inv, float cz) {
+    const float y0 = copysignf(ex2_ftz(fmaf(k, lg2_ftz(fabsf(m0) * inv), cz)), m0);
+    const float y1 = copysignf(ex2_ftz(fmaf(k, lg2_ftz(fabsf(m1) * inv), cz)), m1);
+    return e4m3x2(y0, y1);
+}
+__device__ __forceinline__ uint32_t encode_pair_v(float v0, float v1, float k, float inv, float cz) {
+    return e4m3x2(ex2_ftz(fmaf(k, lg2_ftz(v0 * inv), cz)), ex2_ftz(fmaf(k, lg2_ftz(v1 * inv), cz)));
 }
 
-// Candidate windows around a group's fast extremes (see kFastErr).
-struct Windows {
-    float hi_m, lo_m, hi_v, lo_v;   // |m| >= hi_m, 0 < |m| <= lo_m, v >= hi_v, 0 < v <= lo_v
+// ---------------------------------------------------------------------------
+// G >= 16: CTA-cooperative kernel
+// ---------------------------------------------------------------------------
+
+// Candidate windows of one group, built from its fast statistics.  With
+// T_j = |beta1 m_prev,j| + (1 - beta1)|g_j| <= |m_j| + 2 (1 - beta1)|g_j| and
+// T the same bound over the group, a fast m_j is within eps_m T_j of its
+// exact value and a fast v_j within eps_v v_j, so:
+//   max|m|:  the true max has |m_j| >= fmx_m - 2 eps_m T;
+//   min|m|:  the true smallest non-zero has |m_j| <= fmn_m + eps_m (T_j + T);
+//            and every |m_j| <= 2^10 eps_m T_j (relative error above 2^-10,
+//            where cancellation could move the code by more than one step)
+//            is re-evaluated too;
+//   max v:   v_j >= fmx_v (1 - 2 eps_v);   min v: v_j <= fmn_v (1 + 4 eps_v).
+struct GroupWin {
+    float hi_m, fmn_m, eps_m, T, hi_v, lo_v;
 };
 
-__device__ __forceinline__ Windows windows(const StepArgs& a, float P_m, float mx_m, float mn_m,
-                                           float mx_v, float mn_v, float mx_g) {
-    // m_t may cancel: its error is bounded by kFastErr (beta1 max|m_prev| + (1-beta1) max|g|)
-    const float dm = 2.0f * kFastErr * fmaf(a.beta1, P_m * (1.0f + kFastErr), a.omb1 * mx_g);
-    Windows w;
-    w.hi_m = mx_m - dm;
-    w.lo_m = mn_m > 0.0f ? mn_m + dm : -1.0f;
-    w.hi_v = mx_v * (1.0f - 2.0f * kFastErr);
-    w.lo_v = mn_v > 0.0f ? mn_v * (1.0f + 4.0f * kFastErr) : -1.0f;
+__device__ __forceinline__ GroupWin make_win(const StepArgs& a, float P_m, float eps_m, float eps_v,
+                                             float fmx_m, float fmn_m, float fmx_v, float fmn_v,
+                                             float gmx) {
+    GroupWin w;
+    w.T = fmaf(a.beta1, P_m * (1.0f + eps_m), a.omb1 * gmx);
+    w.eps_m = eps_m;
+    w.hi_m = fmx_m - 2.0f * eps_m * w.T;
+    w.fmn_m = fmn_m;
+    w.hi_v = fmx_v * (1.0f - 2.0f * eps_v);
+    w.lo_v = fmn_v > 0.0f ? fmn_v * (1.0f + 4.0f * eps_v) : -1.0f;
     return w;
 }
 
-__device__ __forceinline__ bool in_window(float x, int s, const Windows& w) {
+// Is an element (|x|, |g|) a candidate of statistic s?
+__device__ __forceinline__ bool cand(float x, float gabs, int s, const GroupWin& w, float omb1) {
     const float ax = fabsf(x);
+    if (!(ax > 0.0f)) return false;
     switch (s) {
-        case 0: return ax >= w.hi_m && ax > 0.0f;
-        case 1: return ax <= w.lo_m && ax > 0.0f;
-        case 2: return ax >= w.hi_v && ax > 0.0f;
-        default: return ax <= w.lo_v && ax > 0.0f;
+        case 0: return ax >= w.hi_m;
+        case 1: {
+            const float Tj = fmaf(2.0f * omb1, gabs, ax);
+            return (w.fmn_m > 0.0f && ax <= fmaf(w.eps_m, Tj + w.T, w.fmn_m)) ||
+                   ax <= 1024.0f * w.eps_m * Tj;
+        }
+        case 2: return ax >= w.hi_v;
+        default: return ax <= w.lo_v;
     }
 }
 
-// ---------------------------------------------------------------------------
-// G >= 32: a group spans L = G/16 lanes
-// ---------------------------------------------------------------------------
-template <int G>
-__global__ void __launch_bounds__(kStepThreads)
-step_kernel_lanes(const StepArgs a) {
-    constexpr int L = G / kVec;
-    static_assert(L >= 2 && L <= 32, "lanes per group");
-    __shared__ StepSmem sm;
-    if (threadIdx.x < 128) {
-        sm.lg_hi[threadIdx.x] = __uint_as_float(kLog2Frac448Hi[threadIdx.x]);
-        sm.lg_lo[threadIdx.x] = __uint_as_float(kLog2Frac448Lo[threadIdx.x]);
-    }
-    load_smem_tables(sm.t, threadIdx.x, kStepThreads);
-    __syncthreads();
-    const df::Tables tab = tables_of(sm.t);
+// Per-group shared-memory record (index of the group within the CTA).
+struct GroupRec {
+    F2 A[2];             // log2(448 S) of the stored m (0) and v (1)
+    F2 rkd[2];           // 1/k
+    float P[2];          // fast-path factor
+    float S[2];          // stored S
+    float eps[2];        // fast-path error bound
+    float fmx[2];        // fast max |m|, max v
+    float fmn[2];        // fast smallest non-zero
+    float gmx;           // max |g|
+    uint32_t hwarp;      // warp holding the group
+    uint32_t holders[4]; // lanes holding candidates, per statistic
+    float ex[4];         // exact extremes
+    F2 lex[4];           // their log2
+    float k[2];          // fresh k
+    float inv[2];        // encoding constants
+    float cz[2];
+};
 
-    const int lane = threadIdx.x & 31;
-    WarpStage& ws = sm.stage[threadIdx.x >> 5];
-    const int64_t base = ((int64_t)blockIdx.x * kStepThreads + threadIdx.x) * kVec;
-    if (__all_sync(kFull, base >= a.n)) return;   // warp-uniform exit
+// Moment rows: 16 floats per thread, the four 16-byte chunks of thread t
+// stored in the order q ^ ((t >> 1) & 3): 128-bit accesses by consecutive
+// threads hit distinct bank groups.
+__device__ __forceinline__ int chunk_slot(int t, int q) { return 4 * (q ^ ((t >> 1) & 3)); }
+
+template <int G>
+struct CtaLayout {
+    static constexpr int NGC = kCtaElems / G;   // groups per CTA
+    static constexpr int L = G / kVec;          // lanes per group
+    static constexpr size_t off_m = 0;
+    static constexpr size_t off_v = off_m + (size_t)kCta * kVec * 4;
+    static constexpr size_t off_grp = off_v + (size_t)kCta * kVec * 4;
+    static constexpr size_t off_lg = off_grp + (size_t)NGC * sizeof(GroupRec);
+    static constexpr size_t off_tab = off_lg + 2 * 128 * 4;
+    static constexpr size_t bytes = off_tab + sizeof(SmemTables);
+};
+
+template <int G>
+__global__ void __launch_bounds__(kCta)
+step_kernel_cta(const StepArgs a) {
+    using Lay = CtaLayout<G>;
+    constexpr int NGC = Lay::NGC;
+    constexpr int L = Lay::L;
+    static_assert(L >= 1 && L <= 16 && (Lay::off_v % 16) == 0 && (Lay::off_grp % 16) == 0 &&
+                      (Lay::off_lg % 4) == 0,
+                  "shared-memory layout");
+    extern __shared__ __align__(16) unsigned char smem[];
+    float(*sm_m)[kVec] = reinterpret_cast<float(*)[kVec]>(smem + Lay::off_m);
+    float(*sm_v)[kVec] = reinterpret_cast<float(*)[kVec]>(smem + Lay::off_v);
+    GroupRec* grp = reinterpret_cast<GroupRec*>(smem + Lay::off_grp);
+    float* lg_hi = reinterpret_cast<float*>(smem + Lay::off_lg);
+    float* lg_lo = lg_hi + 128;
+    SmemTables& st = *reinterpret_cast<SmemTables*>(smem + Lay::off_tab);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t cta_base = (int64_t)blockIdx.x * kCtaElems;
+    const int64_t g_first = cta_base / G;
+    const int64_t base = cta_base + (int64_t)tid * kVec;
     const bool active = base < a.n;
     const bool full = base + kVec <= a.n;
-    const int64_t grp = base / G;
-    const bool group_exists = grp * G < a.n;
-    const int lig = lane % L;          // lane within the group
-    const int gbase = lane - lig;      // first lane of the group
 
+    // this thread's parameters: the loads are in flight during phase B
     Chunk c;
     if (active) load_chunk(a, base, full, c);
     else zero_chunk(c);
 
-    // -- stored-state parameters: even lanes the first moment, odd lanes the second --
-    StateParams pm, pv;
-    {
-        float4 md = make_float4(0.0f, 1.0f, 0.0f, 1.0f);
-        if (group_exists) md = ld_cs(a.meta + grp);
-        const bool odd = lane & 1;
-        const StateParams p = state_params(odd ? md.z : md.x, odd ? md.w : md.y, tab);
-        const int sm_ = lane & ~1, sv_ = lane | 1;
-        pm.A.hi = __shfl_sync(kFull, p.A.hi, sm_);
-        pm.A.lo = __shfl_sync(kFull, p.A.lo, sm_);
-        pm.rkd.hi = __shfl_sync(kFull, p.rkd.hi, sm_);
-        pm.rkd.lo = __shfl_sync(kFull, p.rkd.lo, sm_);
-        pm.P = __shfl_sync(kFull, p.P, sm_);
-        pv.A.hi = __shfl_sync(kFull, p.A.hi, sv_);
-        pv.A.lo = __shfl_sync(kFull, p.A.lo, sv_);
-        pv.rkd.hi = __shfl_sync(kFull, p.rkd.hi, sv_);
-        pv.rkd.lo = __shfl_sync(kFull, p.rkd.lo, sv_);
-        pv.P = __shfl_sync(kFull, p.P, sv_);
+    if (tid < 128) {
+        lg_hi[tid] = __uint_as_float(kLog2Frac448Hi[tid]);
+        lg_lo[tid] = __uint_as_float(kLog2Frac448Lo[tid]);
     }
+    load_smem_tables(st, tid, kCta);
+    __syncthreads();
+    const df::Tables tab = tables_of(st);
 
-    // -- fast path + stage-1 statistics --
-    float m[kVec], v[kVec];
-    float lmx_m, lmx_v, lmx_g;
-    uint32_t lmn_m, lmn_v;
-    fast_path<1, kVec>(a, c, sm.lg_hi, &pm.P, &pm.rkd.hi, &pv.P, &pv.rkd.hi, m, v, &lmx_m, &lmn_m,
-                       &lmx_v, &lmn_v, &lmx_g);
-
-    // publish the fast moments and raw inputs of this lane
-    {
-        float4* pm4 = reinterpret_cast<float4*>(ws.m[lane]);
-        float4* pv4 = reinterpret_cast<float4*>(ws.v[lane]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            pm4[i] = make_float4(m[4 * i], m[4 * i + 1], m[4 * i + 2], m[4 * i + 3]);
-            pv4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    // ---- B: stored-state parameters, one job per (group, moment) ----
+    for (int j = tid; j < 2 * NGC; j += kCta) {
+        const int gi = j >> 1, sm_ = j & 1;
+        const int64_t gg = g_first + gi;
+        float S = 0.0f, k = 1.0f;
+        if (gg * G < a.n) {
+            const float2 sk = reinterpret_cast<const float2*>(a.meta + gg)[sm_];
+            S = sk.x;
+            k = sk.y;
         }
-        *reinterpret_cast<uint4*>(ws.mq[lane]) = make_uint4(c.mq[0], c.mq[1], c.mq[2], c.mq[3]);
-        *reinterpret_cast<uint4*>(ws.vq[lane]) = make_uint4(c.vq[0], c.vq[1], c.vq[2], c.vq[3]);
-        *reinterpret_cast<uint4*>(&ws.g[lane][0]) = make_uint4(c.g[0], c.g[1], c.g[2], c.g[3]);
-        *reinterpret_cast<uint4*>(&ws.g[lane][4]) = make_uint4(c.g[4], c.g[5], c.g[6], c.g[7]);
+        const StateParams p = state_params(S, k, tab);
+        GroupRec& r = grp[gi];
+        r.A[sm_] = p.A;
+        r.rkd[sm_] = p.rkd;
+        r.P[sm_] = p.P;
+        r.S[sm_] = S;
+        r.eps[sm_] = fast_err(p.rkd.hi);
     }
+    __syncthreads();
 
-    // -- stage 2: across the lanes of the group --
-    float mx_m = lmx_m, mx_v = lmx_v, mx_g = lmx_g;
-    uint32_t mn_m = lmn_m, mn_v = lmn_v;
+    // ---- C: fast path, statistics, candidate holders ----
+    const int gi = (tid * kVec) / G;
+    const int lig = (tid * kVec % G) / kVec;   // lane within the group
+    {
+        const GroupRec& r = grp[gi];
+        const float Pm = r.P[0], rkm = r.rkd[0].hi, Pv = r.P[1], rkv = r.rkd[1].hi;
+        float lmx_m = 0.0f, lmx_v = 0.0f, lmx_g = 0.0f;
+        uint32_t lmn_m = 0xFFFFFFFEu, lmn_v = 0xFFFFFFFEu;
 #pragma unroll
-    for (int off = L / 2; off > 0; off >>= 1) {
-        mx_m = fmaxf(mx_m, __shfl_xor_sync(kFull, mx_m, off));
-        mx_v = fmaxf(mx_v, __shfl_xor_sync(kFull, mx_v, off));
-        mx_g = fmaxf(mx_g, __shfl_xor_sync(kFull, mx_g, off));
-        mn_m = min(mn_m, __shfl_xor_sync(kFull, mn_m, off));
-        mn_v = min(mn_v, __shfl_xor_sync(kFull, mn_v, off));
+        for (int q = 0; q < 4; ++q) {
+            float mt[4], vt[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = 4 * q + i;
+                const float gf = bf16_of(c.g, e);
+                fast_elem(a, c.mq[q] >> (8 * i), c.vq[q] >> (8 * i), gf, c.w[e], lg_hi, Pm, rkm,
+                          Pv, rkv, mt[i], vt[i]);
+                lmx_m = fmaxf(lmx_m, fabsf(mt[i]));
+                lmx_v = fmaxf(lmx_v, vt[i]);
+                lmx_g = fmaxf(lmx_g, fabsf(gf));
+                lmn_m = min(lmn_m, min_key(mt[i]));
+                lmn_v = min(lmn_v, min_key(vt[i]));
+            }
+            const int slot = chunk_slot(tid, q);
+            *reinterpret_cast<float4*>(&sm_m[tid][slot]) = make_float4(mt[0], mt[1], mt[2], mt[3]);
+            *reinterpret_cast<float4*>(&sm_v[tid][slot]) = make_float4(vt[0], vt[1], vt[2], vt[3]);
+        }
+        if (active) store_w(a, base, full, c);
+
+        // stage 2 across the lanes of the group
+        float fmx_m = lmx_m, fmx_v = lmx_v, gmx = lmx_g;
+        uint32_t fmn_m = lmn_m, fmn_v = lmn_v;
+#pragma unroll
+        for (int off = L / 2; off > 0; off >>= 1) {
+            fmx_m = fmaxf(fmx_m, __shfl_xor_sync(kFull, fmx_m, off));
+            fmx_v = fmaxf(fmx_v, __shfl_xor_sync(kFull, fmx_v, off));
+            gmx = fmaxf(gmx, __shfl_xor_sync(kFull, gmx, off));
+            fmn_m = min(fmn_m, __shfl_xor_sync(kFull, fmn_m, off));
+            fmn_v = min(fmn_v, __shfl_xor_sync(kFull, fmn_v, off));
+        }
+        const float fmn_mv = min_key_value(fmn_m), fmn_vv = min_key_value(fmn_v);
+        const GroupWin win = make_win(a, Pm, r.eps[0], r.eps[1], fmx_m, fmn_mv, fmx_v, fmn_vv, gmx);
+        // lane-level tests: sufficient conditions for holding a candidate
+        const float lmn_mv = min_key_value(lmn_m);
+        const float Tl = fmaf(2.0f * a.omb1, lmx_g, lmx_m);   // >= T_j of every element here
+        const bool c1 = lmn_mv > 0.0f &&
+                        ((fmn_mv > 0.0f && lmn_mv <= fmaf(win.eps_m, Tl + win.T, fmn_mv)) ||
+                         lmn_mv <= 1024.0f * win.eps_m * Tl);
+        const uint32_t gmask = ((1u << L) - 1u) << (lane - lig);
+        const uint32_t h0 = __ballot_sync(kFull, cand(lmx_m, 0.0f, 0, win, a.omb1)) & gmask;
+        const uint32_t h1 = __ballot_sync(kFull, c1) & gmask;
+        const uint32_t h2 = __ballot_sync(kFull, cand(lmx_v, 0.0f, 2, win, a.omb1)) & gmask;
+        const uint32_t h3 = __ballot_sync(kFull, cand(min_key_value(lmn_v), 0.0f, 3, win, a.omb1)) & gmask;
+        if (lig == 0) {
+            GroupRec& rw = grp[gi];
+            rw.fmx[0] = fmx_m;
+            rw.fmx[1] = fmx_v;
+            rw.fmn[0] = fmn_mv;
+            rw.fmn[1] = fmn_vv;
+            rw.gmx = gmx;
+            rw.hwarp = (uint32_t)warp;
+            rw.holders[0] = h0;
+            rw.holders[1] = h1;
+            rw.holders[2] = h2;
+            rw.holders[3] = h3;
+        }
     }
-    const Windows win = windows(a, pm.P, mx_m, min_key_value(mn_m), mx_v, min_key_value(mn_v), mx_g);
+    __syncthreads();
 
-    // lanes whose local extreme falls in a window hold candidates
-    const uint32_t gmask = (L == 32) ? kFull : (((1u << L) - 1u) << gbase);
-    uint32_t holders[4];
-    holders[0] = __ballot_sync(kFull, in_window(lmx_m, 0, win)) & gmask;
-    holders[1] = __ballot_sync(kFull, in_window(min_key_value(lmn_m), 1, win)) & gmask;
-    holders[2] = __ballot_sync(kFull, in_window(lmx_v, 2, win)) & gmask;
-    holders[3] = __ballot_sync(kFull, in_window(min_key_value(lmn_v), 3, win)) & gmask;
-    __syncwarp();
-
-    // -- exact extremes: lane lig of the group evaluates the statistics s = lig (mod L) --
-    // s: 0 max|m|, 1 smallest non-zero |m|, 2 max v, 3 smallest non-zero v
-    float ex[4];
+    // ---- D: candidates re-evaluated exactly, one job per (group, statistic) ----
+    // A job may read a value another job of the same group has already
+    // replaced by its exact value; the windows hold the exact values of the
+    // true extremes too, so the outcome is the same.
+    for (int j = tid; j < 4 * NGC; j += kCta) {
+        const int jg = j >> 2, s = j & 3;
+        GroupRec& r = grp[jg];
+        const bool second = s >= 2, is_max = (s & 1) == 0;
+        const int sm_ = second ? 1 : 0;
+        const GroupWin win = make_win(a, r.P[0], r.eps[0], r.eps[1], r.fmx[0], r.fmn[0], r.fmx[1],
+                                      r.fmn[1], r.gmx);
+        const F2 A = r.A[sm_], rkd = r.rkd[sm_];
+        const float S = r.S[sm_];
+        const float beta = second ? a.beta2 : a.beta1, omb = second ? a.omb2 : a.omb1;
+        float best = is_max ? 0.0f : kInf;
+        uint32_t h = r.holders[s];
+        while (h) {
+            const int ln = __ffs(h) - 1;
+            h &= h - 1u;
+            const int th = (int)r.hwarp * 32 + ln;
+            const int64_t tb = cta_base + (int64_t)th * kVec;
+            float* vals = second ? sm_v[th] : sm_m[th];
+            // the holder's gradients and codes, read again (this CTA just streamed them)
+            uint32_t gw[8], cw[4];
+            if (tb + kVec <= a.n) {
+                const uint4 g0 = __ldg(reinterpret_cast<const uint4*>(a.g + tb));
+                const uint4 g1 = __ldg(reinterpret_cast<const uint4*>(a.g + tb) + 1);
+                // the codes are rewritten by this kernel (phase F): no read-only path
+                const uint4 cc = __ldcg(reinterpret_cast<const uint4*>((second ? a.vq : a.mq) + tb));
+                gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
+                gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
+                cw[0] = cc.x; cw[1] = cc.y; cw[2] = cc.z; cw[3] = cc.w;
+            } else {
+                for (int i = 0; i < 8; ++i) gw[i] = 0u;
+                for (int i = 0; i < 4; ++i) cw[i] = 0u;
+                for (int e = 0; e < kVec && tb + e < a.n; ++e) {
+                    gw[e / 2] |= (uint32_t)a.g[tb + e] << (16 * (e & 1));
+                    cw[e / 4] |= (uint32_t)(second ? a.vq : a.mq)[tb + e] << (8 * (e & 3));
+                }
+            }
+            uint32_t msk = 0u;
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        const bool is_max = (s & 1) == 0;
-        const bool second = s >= 2;
-        float best = is_max ? 0.0f : __int_as_float(0x7F800000);
-        if (s % L == lig) {
-            const StateParams& sp = second ? pv : pm;
-            uint32_t h = holders[s];
-            while (h) {
-                const int lc = __ffs(h) - 1;
-                h &= h - 1u;
-                const float* vals = second ? ws.v[lc] : ws.m[lc];
-                for (int e = 0; e < kVec; ++e) {
-                    if (!in_window(vals[e], s, win)) continue;
-                    const uint32_t code = byte_of(second ? ws.vq[lc] : ws.mq[lc], e);
-                    const float x = fabsf(exact_moment(code, bf16_of(ws.g[lc], e), second, sp,
-                                                       second ? a.beta2 : a.beta1,
-                                                       second ? a.omb2 : a.omb1, tab, sm.lg_hi,
-                                                       sm.lg_lo));
-                    if (is_max) best = fmaxf(best, x);
-                    else if (x > 0.0f) best = fminf(best, x);
+            for (int q = 0; q < 4; ++q) {
+                const float4 x = *reinterpret_cast<const float4*>(vals + chunk_slot(th, q));
+                msk |= (cand(x.x, fabsf(bf16_of(gw, 4 * q)), s, win, a.omb1) ? 1u : 0u) << (4 * q);
+                msk |= (cand(x.y, fabsf(bf16_of(gw, 4 * q + 1)), s, win, a.omb1) ? 1u : 0u) << (4 * q + 1);
+                msk |= (cand(x.z, fabsf(bf16_of(gw, 4 * q + 2)), s, win, a.omb1) ? 1u : 0u) << (4 * q + 2);
+                msk |= (cand(x.w, fabsf(bf16_of(gw, 4 * q + 3)), s, win, a.omb1) ? 1u : 0u) << (4 * q + 3);
+            }
+            while (msk) {
+                const int e = __ffs(msk) - 1;
+                msk &= msk - 1u;
+                const float x = exact_moment(byte_of(cw, e), bf16_of(gw, e), second, A, rkd, S,
+                                             beta, omb, tab, lg_hi, lg_lo);
+                vals[chunk_slot(th, e >> 2) + (e & 3)] = x;   // encoded from the exact value
+                const float ax = fabsf(x);
+                if (is_max) best = fmaxf(best, ax);
+                else if (ax > 0.0f) best = fminf(best, ax);
+            }
+        }
+        best = (best < kInf) ? best : 0.0f;
+        r.ex[s] = best;
+        r.lex[s] = best > 0.0f ? df::log2_df(best, tab) : F2{0.0f, 0.0f};
+    }
+    __syncthreads();
+
+    // ---- E: fresh k, S, encoding constants and the group record ----
+    for (int j = tid; j < 2 * NGC; j += kCta) {
+        const int jg = j >> 1, sm_ = j & 1;
+        GroupRec& r = grp[jg];
+        const float mx = r.ex[2 * sm_], mn = r.ex[2 * sm_ + 1];
+        float k, S;
+        k_and_S_logs(mx, mn, r.lex[2 * sm_], r.lex[2 * sm_ + 1], tab, k, S);
+        float inv, cz;
+        encode_consts(mx, k, inv, cz);
+        r.k[sm_] = k;
+        r.inv[sm_] = inv;
+        r.cz[sm_] = cz;
+        const int64_t gg = g_first + jg;
+        if (gg * G < a.n) reinterpret_cast<float2*>(a.meta + gg)[sm_] = make_float2(S, k);
+    }
+    __syncthreads();
+
+    // ---- F: encode and store the codes ----
+    if (!active) return;
+    {
+        const GroupRec& r = grp[gi];
+        const float km = r.k[0], invm = r.inv[0], czm = r.cz[0];
+        const float kv = r.k[1], invv = r.inv[1], czv = r.cz[1];
+        uint32_t om[4], ov[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int slot = chunk_slot(tid, q);
+            const float4 m4 = *reinterpret_cast<const float4*>(&sm_m[tid][slot]);
+            const float4 v4 = *reinterpret_cast<const float4*>(&sm_v[tid][slot]);
+            om[q] = encode_pair_m(m4.x, m4.y, km, invm, czm) | (encode_pair_m(m4.z, m4.w, km, invm, czm) << 16);
+            ov[q] = encode_pair_v(v4.x, v4.y, kv, invv, czv) | (encode_pair_v(v4.z, v4.w, kv, invv, czv) << 16);
+        }
+        if (full) {
+            st_cs(reinterpret_cast<uint4*>(a.mq + base), make_uint4(om[0], om[1], om[2], om[3]));
+            st_cs(reinterpret_cast<uint4*>(a.vq + base), make_uint4(ov[0], ov[1], ov[2], ov[3]));
+        } else {
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) {
+                if (base + e < a.n) {
+                    a.mq[base + e] = (uint8_t)(om[e / 4] >> (8 * (e & 3)));
+                    a.vq[base + e] = (uint8_t)(ov[e / 4] >> (8 * (e & 3)));
                 }
             }
         }
-        ex[s] = best;
     }
-    __syncwarp();
-#pragma unroll
-    for (int s = 0; s < 4; ++s) ex[s] = __shfl_sync(kFull, ex[s], gbase + s % L);
-    if (!(ex[1] < __int_as_float(0x7F800000))) ex[1] = 0.0f;
-    if (!(ex[3] < __int_as_float(0x7F800000))) ex[3] = 0.0f;
-
-    // -- fresh (k, S): even lanes the first moment, odd lanes the second --
-    float k_m, S_m, k_v, S_v;
-    {
-        const bool odd = lane & 1;
-        const float mx = odd ? ex[2] : ex[0];
-        const float mn = odd ? ex[3] : ex[1];
-        const F2 Lmx = mx > 0.0f ? df::log2_df(mx, tab) : F2{0.0f, 0.0f};
-        const F2 Lmn = (mn > 0.0f && mn < mx) ? df::log2_df(mn, tab) : F2{0.0f, 0.0f};
-        float kk, SS;
-        k_and_S(mx, mn, Lmx, Lmn, tab, kk, SS);
-        k_m = __shfl_sync(kFull, kk, lane & ~1);
-        S_m = __shfl_sync(kFull, SS, lane & ~1);
-        k_v = __shfl_sync(kFull, kk, lane | 1);
-        S_v = __shfl_sync(kFull, SS, lane | 1);
-    }
-    if (!active) return;
-
-    const EncodeParams em = encode_params(ex[0], k_m);
-    const EncodeParams ev = encode_params(ex[2], k_v);
-    encode_store<1, kVec>(a, base, full, c, m, v, &em, &ev);
-    if (lig == 0) st_cs(a.meta + grp, make_float4(S_m, k_m, S_v, k_v));
 }
 
 // ---------------------------------------------------------------------------
-// G <= 16: a thread holds 16/G whole groups
+// G < 16: a thread holds 16/G whole groups (the same arithmetic, per thread)
 // ---------------------------------------------------------------------------
+constexpr int kThreadCta = 128;
+
 template <int G>
-__global__ void __launch_bounds__(kStepThreads)
+__global__ void __launch_bounds__(kThreadCta)
 step_kernel_thread(const StepArgs a) {
     constexpr int NG = kVec / G;
-    constexpr int E = G;
     __shared__ float lg_hi[128], lg_lo[128];
     __shared__ SmemTables st;
     if (threadIdx.x < 128) {
         lg_hi[threadIdx.x] = __uint_as_float(kLog2Frac448Hi[threadIdx.x]);
         lg_lo[threadIdx.x] = __uint_as_float(kLog2Frac448Lo[threadIdx.x]);
     }
-    load_smem_tables(st, threadIdx.x, kStepThreads);
+    load_smem_tables(st, threadIdx.x, kThreadCta);
     __syncthreads();
     const df::Tables tab = tables_of(st);
 
-    const int64_t base = ((int64_t)blockIdx.x * kStepThreads + threadIdx.x) * kVec;
+    const int64_t base = ((int64_t)blockIdx.x * kThreadCta + threadIdx.x) * kVec;
     if (base >= a.n) return;
     const bool full = base + kVec <= a.n;
     const int64_t g0 = base / G;
 
     Chunk c;
     load_chunk(a, base, full, c);
-    StateParams pm[NG], pv[NG];
-    float Pm[NG], Pv[NG], rkm[NG], rkv[NG];
+    float m[kVec], v[kVec];
+    float km[NG], kv[NG], Sm[NG], Sv[NG], inv_m[NG], cz_m[NG], inv_v[NG], cz_v[NG];
 #pragma unroll
     for (int j = 0; j < NG; ++j) {
         float4 md = make_float4(0.0f, 1.0f, 0.0f, 1.0f);
         if ((g0 + j) * G < a.n) md = ld_cs(a.meta + g0 + j);
-        pm[j] = state_params(md.x, md.y, tab);
-        pv[j] = state_params(md.z, md.w, tab);
-        Pm[j] = pm[j].P; rkm[j] = pm[j].rkd.hi; Pv[j] = pv[j].P; rkv[j] = pv[j].rkd.hi;
-    }
-    float m[kVec], v[kVec];
-    float mx_m[NG], mx_v[NG], mx_g[NG];
-    uint32_t mn_m[NG], mn_v[NG];
-    fast_path<NG, E>(a, c, lg_hi, Pm, rkm, Pv, rkv, m, v, mx_m, mn_m, mx_v, mn_v, mx_g);
-
-    EncodeParams em[NG], ev[NG];
-    float k_m[NG], S_m[NG], k_v[NG], S_v[NG];
+        const StateParams pm = state_params(md.x, md.y, tab);
+        const StateParams pv = state_params(md.z, md.w, tab);
+        const float eps_m = fast_err(pm.rkd.hi), eps_v = fast_err(pv.rkd.hi);
+        float fmx_m = 0.0f, fmx_v = 0.0f, gmx = 0.0f;
+        uint32_t fmn_m = 0xFFFFFFFEu, fmn_v = 0xFFFFFFFEu;
 #pragma unroll
-    for (int j = 0; j < NG; ++j) {
-        const Windows win = windows(a, Pm[j], mx_m[j], min_key_value(mn_m[j]), mx_v[j],
-                                    min_key_value(mn_v[j]), mx_g[j]);
-        float ex[4];
+        for (int i = 0; i < G; ++i) {
+            const int e = j * G + i;
+            const float gf = bf16_of(c.g, e);
+            fast_elem(a, byte_of(c.mq, e), byte_of(c.vq, e), gf, c.w[e], lg_hi, pm.P, pm.rkd.hi,
+                      pv.P, pv.rkd.hi, m[e], v[e]);
+            fmx_m = fmaxf(fmx_m, fabsf(m[e]));
+            fmx_v = fmaxf(fmx_v, v[e]);
+            gmx = fmaxf(gmx, fabsf(gf));
+            fmn_m = min(fmn_m, min_key(m[e]));
+            fmn_v = min(fmn_v, min_key(v[e]));
+        }
+        const GroupWin win = make_win(a, pm.P, eps_m, eps_v, fmx_m, min_key_value(fmn_m), fmx_v,
+                                      min_key_value(fmn_v), gmx);
+        float ex[4] = {0.0f, kInf, 0.0f, kInf};
+        // every element inside any window is re-evaluated once and encoded exactly
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            const bool is_max = (s & 1) == 0;
-            const bool second = s >= 2;
-            float best = is_max ? 0.0f : __int_as_float(0x7F800000);
-#pragma unroll
-            for (int ee = 0; ee < E; ++ee) {
-                const int e = j * E + ee;
-                if (!in_window(second ? v[e] : m[e], s, win)) continue;
-                const float x = fabsf(exact_moment(byte_of(second ? c.vq : c.mq, e), bf16_of(c.g, e),
-                                                   second, second ? pv[j] : pm[j],
-                                                   second ? a.beta2 : a.beta1,
-                                                   second ? a.omb2 : a.omb1, tab, lg_hi, lg_lo));
-                if (is_max) best = fmaxf(best, x);
-                else if (x > 0.0f) best = fminf(best, x);
+        for (int i = 0; i < G; ++i) {
+            const int e = j * G + i;
+            const float gf = bf16_of(c.g, e);
+            const bool cm = cand(m[e], fabsf(gf), 0, win, a.omb1) || cand(m[e], fabsf(gf), 1, win, a.omb1);
+            const bool cv = cand(v[e], 0.0f, 2, win, a.omb1) || cand(v[e], 0.0f, 3, win, a.omb1);
+            if (cm) {
+                m[e] = exact_moment(byte_of(c.mq, e), gf, false, pm.A, pm.rkd, pm.S, a.beta1,
+                                    a.omb1, tab, lg_hi, lg_lo);
+                const float ax = fabsf(m[e]);
+                ex[0] = fmaxf(ex[0], ax);
+                if (ax > 0.0f) ex[1] = fminf(ex[1], ax);
             }
-            ex[s] = best;
+            if (cv) {
+                v[e] = exact_moment(byte_of(c.vq, e), gf, true, pv.A, pv.rkd, pv.S, a.beta2,
+                                    a.omb2, tab, lg_hi, lg_lo);
+                const float ax = fabsf(v[e]);
+                ex[2] = fmaxf(ex[2], ax);
+                if (ax > 0.0f) ex[3] = fminf(ex[3], ax);
+            }
         }
-        if (!(ex[1] < __int_as_float(0x7F800000))) ex[1] = 0.0f;
-        if (!(ex[3] < __int_as_float(0x7F800000))) ex[3] = 0.0f;
-#pragma unroll
-        for (int st2 = 0; st2 < 2; ++st2) {
-            const float mx = ex[2 * st2], mn = ex[2 * st2 + 1];
-            const F2 Lmx = mx > 0.0f ? df::log2_df(mx, tab) : F2{0.0f, 0.0f};
-            const F2 Lmn = (mn > 0.0f && mn < mx) ? df::log2_df(mn, tab) : F2{0.0f, 0.0f};
-            if (st2 == 0) k_and_S(mx, mn, Lmx, Lmn, tab, k_m[j], S_m[j]);
-            else k_and_S(mx, mn, Lmx, Lmn, tab, k_v[j], S_v[j]);
-        }
-        em[j] = encode_params(ex[0], k_m[j]);
-        ev[j] = encode_params(ex[2], k_v[j]);
+        if (!(ex[1] < kInf)) ex[1] = 0.0f;
+        if (!(ex[3] < kInf)) ex[3] = 0.0f;
+        k_and_S(ex[0], ex[1], tab, km[j], Sm[j]);
+        k_and_S(ex[2], ex[3], tab, kv[j], Sv[j]);
+        encode_consts(ex[0], km[j], inv_m[j], cz_m[j]);
+        encode_consts(ex[2], kv[j], inv_v[j], cz_v[j]);
     }
-    encode_store<NG, E>(a, base, full, c, m, v, em, ev);
+    store_w(a, base, full, c);
+    uint32_t om[4], ov[4];
+#pragma unroll
+    for (int e = 0; e < kVec; e += 2) {
+        const int j0 = e / G, j1 = (e + 1) / G;
+        const float ym0 = copysignf(ex2_ftz(fmaf(km[j0], lg2_ftz(fabsf(m[e]) * inv_m[j0]), cz_m[j0])), m[e]);
+        const float ym1 = copysignf(ex2_ftz(fmaf(km[j1], lg2_ftz(fabsf(m[e + 1]) * inv_m[j1]), cz_m[j1])), m[e + 1]);
+        const float yv0 = ex2_ftz(fmaf(kv[j0], lg2_ftz(v[e] * inv_v[j0]), cz_v[j0]));
+        const float yv1 = ex2_ftz(fmaf(kv[j1], lg2_ftz(v[e + 1] * inv_v[j1]), cz_v[j1]));
+        const uint32_t pm_ = e4m3x2(ym0, ym1), pv_ = e4m3x2(yv0, yv1);
+        if ((e & 2) == 0) { om[e / 4] = pm_; ov[e / 4] = pv_; }
+        else { om[e / 4] |= pm_ << 16; ov[e / 4] |= pv_ << 16; }
+    }
+    if (full) {
+        st_cs(reinterpret_cast<uint4*>(a.mq + base), make_uint4(om[0], om[1], om[2], om[3]));
+        st_cs(reinterpret_cast<uint4*>(a.vq + base), make_uint4(ov[0], ov[1], ov[2], ov[3]));
+    } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            if (base + e < a.n) {
+                a.mq[base + e] = (uint8_t)(om[e / 4] >> (8 * (e & 3)));
+                a.vq[base + e] = (uint8_t)(ov[e / 4] >> (8 * (e & 3)));
+            }
+        }
+    }
 #pragma unroll
     for (int j = 0; j < NG; ++j)
-        if ((g0 + j) * G < a.n) st_cs(a.meta + g0 + j, make_float4(S_m[j], k_m[j], S_v[j], k_v[j]));
+        if ((g0 + j) * G < a.n) st_cs(a.meta + g0 + j, make_float4(Sm[j], km[j], Sv[j], kv[j]));
 }
 
 template <int G>
 cudaError_t launch_step(const StepArgs& a, cudaStream_t stream) {
-    const int64_t threads = (a.n + kVec - 1) / kVec;
-    const int64_t blocks = (threads + kStepThreads - 1) / kStepThreads;
-    if constexpr (G >= 2 * kVec)
-        step_kernel_lanes<G><<<(unsigned)blocks, kStepThreads, 0, stream>>>(a);
-    else
-        step_kernel_thread<G><<<(unsigned)blocks, kStepThreads, 0, stream>>>(a);
+    if constexpr (G >= kVec) {
+        using Lay = CtaLayout<G>;
+        // more than 48 KB of dynamic shared memory needs the opt-in attribute
+        const cudaError_t e = cudaFuncSetAttribute(step_kernel_cta<G>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)Lay::bytes);
+        if (e != cudaSuccess) return e;
+        const int64_t blocks = (a.n + kCtaElems - 1) / kCtaElems;
+        step_kernel_cta<G><<<(unsigned)blocks, kCta, Lay::bytes, stream>>>(a);
+    } else {
+        const int64_t threads = (a.n + kVec - 1) / kVec;
+        const int64_t blocks = (threads + kThreadCta - 1) / kThreadCta;
+        step_kernel_thread<G><<<(unsigned)blocks, kThreadCta, 0, stream>>>(a);
+    }
     return cudaGetLastError();
 }
 
