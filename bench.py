@@ -31,7 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "FP8 AdamW+DRE step: params/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL = "adamw_dre_step_kernel"
+KERNEL = "step_kernel_cta"
 
 
 def parse():

@@ -53,8 +53,10 @@ namespace {
 using df::F2;
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kCta = 256;                  // threads per CTA
-constexpr int kCtaElems = kCta * kVec;     // parameters per CTA
+#ifndef COAT_STEP_CTA
+#define COAT_STEP_CTA 256
+#endif
+constexpr int kStepCta = COAT_STEP_CTA;    // threads per CTA of the cooperative kernel
 #define kInf __int_as_float(0x7F800000)
 
 // Relative error bound of the SFU exp2 (ex2.approx.ftz.f32), with margin.
@@ -244,25 +246,53 @@ __device__ __forceinline__ void encode_consts(float mx, float k, float& inv, flo
     cz = sub ? fmaf(24.0f, k, kLog2_448) : kLog2_448;
 }
 
-// Smallest-non-zero keys: 2 * bits(|x|) - 2 as unsigned drops the sign and
-// sends +-0 to 0xFFFFFFFE, above every non-zero magnitude.
-__device__ __forceinline__ uint32_t min_key(float x) { return __float_as_uint(x) * 2u - 2u; }
-__device__ __forceinline__ float min_key_value(uint32_t k) {
-    return k >= 0xFFFFFFFEu ? 0.0f : __uint_as_float((k + 2u) >> 1);
+// Three-input minimum / maximum (PTX min/max with three operands, sm_100 and
+// later).  A NaN operand is ignored unless every operand is NaN.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
-// Fast path of one element: dequantize, EMAs, AdamW.  The code's sign goes
-// onto P, and the "+ 0" keeps a zero magnitude at +0 whatever the sign bit;
-// SFU ops flush below 2^-126 only.
+// Smallest-non-zero keys: |bits(x) - 1| read as a float orders like |x| for
+// x != 0 and is NaN for +-0, which min ignores.  A minimum of keys started at
+// +inf stays +inf when every value is zero.
+__device__ __forceinline__ float nz_key(float x) {
+    return fabsf(__uint_as_float(__float_as_uint(x) - 1u));
+}
+__device__ __forceinline__ float nz_key_value(float k) {
+    return k < kInf ? __uint_as_float(__float_as_uint(k) + 1u) : 0.0f;
+}
+
+// Byte offset of the table entry of code byte i of a packed word (magnitude
+// bits only): ((w >> 8i) & 0x7F) * 4 with one shift and one mask.
+template <int I>
+__device__ __forceinline__ uint32_t code_off(uint32_t w) {
+    if constexpr (I == 0) return (w << 2) & 0x1FCu;
+    else return (w >> (8 * I - 2)) & 0x1FCu;
+}
+__device__ __forceinline__ float table_at(const float* t, uint32_t off) {
+    return *reinterpret_cast<const float*>(reinterpret_cast<const char*>(t) + off);
+}
+
+// Fast path of one element: dequantize, EMAs, AdamW.  bPm = beta1 P_m and
+// bPv = beta2 P_v per group; the first moment's code sign flips bPm, and
+// (1 - beta1) g is formed as fma(.., .., +0) so that m_t is never -0.  SFU
+// ops flush below 2^-126 only.
+template <int I>
 __device__ __forceinline__ void fast_elem(const StepArgs& a, uint32_t wm, uint32_t wv, float gf,
-                                          float& w, const float* lg, float Pm, float rkm,
-                                          float Pv, float rkv, float& mt, float& vt) {
-    const float em = ex2_ftz(__fmul_rn(lg[wm & 0x7Fu], rkm));
-    const float Ps = __uint_as_float(__float_as_uint(Pm) | ((wm & 0x80u) << 24));
-    const float m_prev = fmaf(em, Ps, 0.0f);
-    const float v_prev = __fmul_rn(Pv, ex2_ftz(__fmul_rn(lg[wv & 0x7Fu], rkv)));
-    mt = fmaf(a.beta1, m_prev, __fmul_rn(a.omb1, gf));
-    vt = fmaf(a.beta2, v_prev, __fmul_rn(__fmul_rn(a.omb2, gf), gf));
+                                          float& w, const float* lg, float bPm, float rkm,
+                                          float bPv, float rkv, float& mt, float& vt) {
+    const float em = ex2_ftz(__fmul_rn(table_at(lg, code_off<I>(wm)), rkm));
+    const float ev = ex2_ftz(__fmul_rn(table_at(lg, code_off<I>(wv)), rkv));
+    const float bPs = __uint_as_float(__float_as_uint(bPm) ^ ((wm << (24 - 8 * I)) & 0x80000000u));
+    mt = fmaf(bPs, em, fmaf(a.omb1, gf, 0.0f));
+    vt = fmaf(bPv, ev, __fmul_rn(__fmul_rn(a.omb2, gf), gf));
     const float denom = __fadd_rn(sqrt_ftz(__fmul_rn(vt, a.c2)), a.eps);
     w = fmaf(__fmul_rn(-a.c1, mt), rcp_ftz(denom), __fmul_rn(w, a.decay));
 }
@@ -307,20 +337,37 @@ __device__ __forceinline__ GroupWin make_win(const StepArgs& a, float P_m, float
     return w;
 }
 
-// Is an element (|x|, |g|) a candidate of statistic s?
-__device__ __forceinline__ bool cand(float x, float gabs, int s, const GroupWin& w, float omb1) {
+// Candidate test of statistic s as one branch-free expression (a job's lanes
+// run different statistics): max statistics test |x| >= hi; min statistics
+// test |x| <= max(a0 + a1 T_j, a2 T_j) with T_j = |x| + c |g| (c = 2(1-beta1)
+// for m, 0 for v).
+struct CandTest {
+    bool is_max;
+    float hi, a0, a1, a2, c;
+};
+
+__device__ __forceinline__ CandTest cand_test(const GroupWin& w, int s, float omb1) {
+    CandTest t;
+    t.is_max = (s & 1) == 0;
+    t.hi = (s == 0) ? w.hi_m : w.hi_v;
+    const bool m_min = (s == 1);
+    t.a0 = m_min ? (w.fmn_m > 0.0f ? fmaf(w.eps_m, w.T, w.fmn_m) : -kInf) : w.lo_v;
+    t.a1 = m_min ? w.eps_m : 0.0f;
+    t.a2 = m_min ? 1024.0f * w.eps_m : 0.0f;
+    t.c = m_min ? 2.0f * omb1 : 0.0f;
+    return t;
+}
+
+// `code` is the element's stored code byte.  A fast value of exactly zero is
+// tested too unless the element's inputs are both zero (g = 0 and a zero
+// code, whose moment is exactly 0): the fast sum can cancel to 0 where the
+// exact one does not, and an SFU flush can zero a tiny non-zero term.
+__device__ __forceinline__ bool cand(float x, float gabs, uint32_t code, const CandTest& t) {
     const float ax = fabsf(x);
-    if (!(ax > 0.0f)) return false;
-    switch (s) {
-        case 0: return ax >= w.hi_m;
-        case 1: {
-            const float Tj = fmaf(2.0f * omb1, gabs, ax);
-            return (w.fmn_m > 0.0f && ax <= fmaf(w.eps_m, Tj + w.T, w.fmn_m)) ||
-                   ax <= 1024.0f * w.eps_m * Tj;
-        }
-        case 2: return ax >= w.hi_v;
-        default: return ax <= w.lo_v;
-    }
+    const float Tj = fmaf(t.c, gabs, ax);
+    const float lo = fmaxf(fmaf(t.a1, Tj, t.a0), t.a2 * Tj);
+    const bool live = ax > 0.0f || gabs > 0.0f || (code & 0x7Fu) != 0u;
+    return live && (t.is_max ? ax >= t.hi : ax <= lo);
 }
 
 // Per-group shared-memory record (index of the group within the CTA).
@@ -347,22 +394,25 @@ struct GroupRec {
 // threads hit distinct bank groups.
 __device__ __forceinline__ int chunk_slot(int t, int q) { return 4 * (q ^ ((t >> 1) & 3)); }
 
-template <int G>
+template <int G, int CTA>
 struct CtaLayout {
+    static constexpr int kCtaElems = CTA * kVec;  // parameters per CTA
     static constexpr int NGC = kCtaElems / G;   // groups per CTA
     static constexpr int L = G / kVec;          // lanes per group
     static constexpr size_t off_m = 0;
-    static constexpr size_t off_v = off_m + (size_t)kCta * kVec * 4;
-    static constexpr size_t off_grp = off_v + (size_t)kCta * kVec * 4;
+    static constexpr size_t off_v = off_m + (size_t)CTA * kVec * 4;
+    static constexpr size_t off_grp = off_v + (size_t)CTA * kVec * 4;
     static constexpr size_t off_lg = off_grp + (size_t)NGC * sizeof(GroupRec);
     static constexpr size_t off_tab = off_lg + 2 * 128 * 4;
     static constexpr size_t bytes = off_tab + sizeof(SmemTables);
 };
 
-template <int G>
-__global__ void __launch_bounds__(kCta)
+template <int G, int CTA>
+__global__ void __launch_bounds__(CTA, 1024 / CTA)   // 64 registers: 1024 threads per SM
 step_kernel_cta(const StepArgs a) {
-    using Lay = CtaLayout<G>;
+    using Lay = CtaLayout<G, CTA>;
+    constexpr int kCta = CTA;
+    constexpr int kCtaElems = Lay::kCtaElems;
     constexpr int NGC = Lay::NGC;
     constexpr int L = Lay::L;
     static_assert(L >= 1 && L <= 16 && (Lay::off_v % 16) == 0 && (Lay::off_grp % 16) == 0 &&
@@ -421,24 +471,27 @@ step_kernel_cta(const StepArgs a) {
     const int lig = (tid * kVec % G) / kVec;   // lane within the group
     {
         const GroupRec& r = grp[gi];
-        const float Pm = r.P[0], rkm = r.rkd[0].hi, Pv = r.P[1], rkv = r.rkd[1].hi;
+        const float Pm = r.P[0], rkm = r.rkd[0].hi, rkv = r.rkd[1].hi;
+        const float bPm = a.beta1 * Pm, bPv = a.beta2 * r.P[1];
         float lmx_m = 0.0f, lmx_v = 0.0f, lmx_g = 0.0f;
-        uint32_t lmn_m = 0xFFFFFFFEu, lmn_v = 0xFFFFFFFEu;
+        float lmn_m = kInf, lmn_v = kInf;   // smallest non-zero, as keys
+        float lz = kInf;                    // smallest |m| or v, zeros included
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float mt[4], vt[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int e = 4 * q + i;
-                const float gf = bf16_of(c.g, e);
-                fast_elem(a, c.mq[q] >> (8 * i), c.vq[q] >> (8 * i), gf, c.w[e], lg_hi, Pm, rkm,
-                          Pv, rkv, mt[i], vt[i]);
-                lmx_m = fmaxf(lmx_m, fabsf(mt[i]));
-                lmx_v = fmaxf(lmx_v, vt[i]);
-                lmx_g = fmaxf(lmx_g, fabsf(gf));
-                lmn_m = min(lmn_m, min_key(mt[i]));
-                lmn_v = min(lmn_v, min_key(vt[i]));
-            }
+            const float g0 = bf16_of(c.g, 4 * q), g1 = bf16_of(c.g, 4 * q + 1);
+            const float g2 = bf16_of(c.g, 4 * q + 2), g3 = bf16_of(c.g, 4 * q + 3);
+            fast_elem<0>(a, c.mq[q], c.vq[q], g0, c.w[4 * q], lg_hi, bPm, rkm, bPv, rkv, mt[0], vt[0]);
+            fast_elem<1>(a, c.mq[q], c.vq[q], g1, c.w[4 * q + 1], lg_hi, bPm, rkm, bPv, rkv, mt[1], vt[1]);
+            fast_elem<2>(a, c.mq[q], c.vq[q], g2, c.w[4 * q + 2], lg_hi, bPm, rkm, bPv, rkv, mt[2], vt[2]);
+            fast_elem<3>(a, c.mq[q], c.vq[q], g3, c.w[4 * q + 3], lg_hi, bPm, rkm, bPv, rkv, mt[3], vt[3]);
+            lmx_g = fmax3(fmax3(lmx_g, fabsf(g0), fabsf(g1)), fabsf(g2), fabsf(g3));
+            lmx_m = fmax3(fmax3(lmx_m, fabsf(mt[0]), fabsf(mt[1])), fabsf(mt[2]), fabsf(mt[3]));
+            lmx_v = fmax3(fmax3(lmx_v, vt[0], vt[1]), vt[2], vt[3]);
+            lmn_m = fmin3(fmin3(lmn_m, nz_key(mt[0]), nz_key(mt[1])), nz_key(mt[2]), nz_key(mt[3]));
+            lmn_v = fmin3(fmin3(lmn_v, nz_key(vt[0]), nz_key(vt[1])), nz_key(vt[2]), nz_key(vt[3]));
+            lz = fmin3(fmin3(lz, fabsf(mt[0]), fabsf(mt[1])), fabsf(mt[2]), fabsf(mt[3]));
+            lz = fmin3(fmin3(lz, vt[0], vt[1]), vt[2], vt[3]);
             const int slot = chunk_slot(tid, q);
             *reinterpret_cast<float4*>(&sm_m[tid][slot]) = make_float4(mt[0], mt[1], mt[2], mt[3]);
             *reinterpret_cast<float4*>(&sm_v[tid][slot]) = make_float4(vt[0], vt[1], vt[2], vt[3]);
@@ -446,29 +499,32 @@ step_kernel_cta(const StepArgs a) {
         if (active) store_w(a, base, full, c);
 
         // stage 2 across the lanes of the group
-        float fmx_m = lmx_m, fmx_v = lmx_v, gmx = lmx_g;
-        uint32_t fmn_m = lmn_m, fmn_v = lmn_v;
+        float fmx_m = lmx_m, fmx_v = lmx_v, gmx = lmx_g, fmn_m = lmn_m, fmn_v = lmn_v;
 #pragma unroll
         for (int off = L / 2; off > 0; off >>= 1) {
             fmx_m = fmaxf(fmx_m, __shfl_xor_sync(kFull, fmx_m, off));
             fmx_v = fmaxf(fmx_v, __shfl_xor_sync(kFull, fmx_v, off));
             gmx = fmaxf(gmx, __shfl_xor_sync(kFull, gmx, off));
-            fmn_m = min(fmn_m, __shfl_xor_sync(kFull, fmn_m, off));
-            fmn_v = min(fmn_v, __shfl_xor_sync(kFull, fmn_v, off));
+            fmn_m = fminf(fmn_m, __shfl_xor_sync(kFull, fmn_m, off));
+            fmn_v = fminf(fmn_v, __shfl_xor_sync(kFull, fmn_v, off));
         }
-        const float fmn_mv = min_key_value(fmn_m), fmn_vv = min_key_value(fmn_v);
+        const float fmn_mv = nz_key_value(fmn_m), fmn_vv = nz_key_value(fmn_v);
         const GroupWin win = make_win(a, Pm, r.eps[0], r.eps[1], fmx_m, fmn_mv, fmx_v, fmn_vv, gmx);
-        // lane-level tests: sufficient conditions for holding a candidate
-        const float lmn_mv = min_key_value(lmn_m);
+        // lane-level tests: sufficient conditions for holding a candidate.  A
+        // lane with a fast zero holds one when the group has a non-zero input.
+        const bool live_m = win.T > 0.0f, live_v = r.P[1] > 0.0f || gmx > 0.0f;
+        const float lmn_mv = nz_key_value(lmn_m), lmn_vv = nz_key_value(lmn_v);
         const float Tl = fmaf(2.0f * a.omb1, lmx_g, lmx_m);   // >= T_j of every element here
-        const bool c1 = lmn_mv > 0.0f &&
-                        ((fmn_mv > 0.0f && lmn_mv <= fmaf(win.eps_m, Tl + win.T, fmn_mv)) ||
-                         lmn_mv <= 1024.0f * win.eps_m * Tl);
+        const bool c1 = (lmn_mv > 0.0f &&
+                         ((fmn_mv > 0.0f && lmn_mv <= fmaf(win.eps_m, Tl + win.T, fmn_mv)) ||
+                          lmn_mv <= 1024.0f * win.eps_m * Tl)) ||
+                        (lz == 0.0f && live_m);
         const uint32_t gmask = ((1u << L) - 1u) << (lane - lig);
-        const uint32_t h0 = __ballot_sync(kFull, cand(lmx_m, 0.0f, 0, win, a.omb1)) & gmask;
+        const uint32_t h0 = __ballot_sync(kFull, lmx_m >= win.hi_m && (lmx_m > 0.0f || live_m)) & gmask;
         const uint32_t h1 = __ballot_sync(kFull, c1) & gmask;
-        const uint32_t h2 = __ballot_sync(kFull, cand(lmx_v, 0.0f, 2, win, a.omb1)) & gmask;
-        const uint32_t h3 = __ballot_sync(kFull, cand(min_key_value(lmn_v), 0.0f, 3, win, a.omb1)) & gmask;
+        const uint32_t h2 = __ballot_sync(kFull, lmx_v >= win.hi_v && (lmx_v > 0.0f || live_v)) & gmask;
+        const uint32_t h3 = __ballot_sync(kFull, (lmn_vv > 0.0f && lmn_vv <= win.lo_v) ||
+                                                     (lz == 0.0f && live_v)) & gmask;
         if (lig == 0) {
             GroupRec& rw = grp[gi];
             rw.fmx[0] = fmx_m;
@@ -496,6 +552,7 @@ step_kernel_cta(const StepArgs a) {
         const int sm_ = second ? 1 : 0;
         const GroupWin win = make_win(a, r.P[0], r.eps[0], r.eps[1], r.fmx[0], r.fmn[0], r.fmx[1],
                                       r.fmn[1], r.gmx);
+        const CandTest ct = cand_test(win, s, a.omb1);
         const F2 A = r.A[sm_], rkd = r.rkd[sm_];
         const float S = r.S[sm_];
         const float beta = second ? a.beta2 : a.beta1, omb = second ? a.omb2 : a.omb1;
@@ -529,10 +586,10 @@ step_kernel_cta(const StepArgs a) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float4 x = *reinterpret_cast<const float4*>(vals + chunk_slot(th, q));
-                msk |= (cand(x.x, fabsf(bf16_of(gw, 4 * q)), s, win, a.omb1) ? 1u : 0u) << (4 * q);
-                msk |= (cand(x.y, fabsf(bf16_of(gw, 4 * q + 1)), s, win, a.omb1) ? 1u : 0u) << (4 * q + 1);
-                msk |= (cand(x.z, fabsf(bf16_of(gw, 4 * q + 2)), s, win, a.omb1) ? 1u : 0u) << (4 * q + 2);
-                msk |= (cand(x.w, fabsf(bf16_of(gw, 4 * q + 3)), s, win, a.omb1) ? 1u : 0u) << (4 * q + 3);
+                msk |= (cand(x.x, fabsf(bf16_of(gw, 4 * q)), byte_of(cw, 4 * q), ct) ? 1u : 0u) << (4 * q);
+                msk |= (cand(x.y, fabsf(bf16_of(gw, 4 * q + 1)), byte_of(cw, 4 * q + 1), ct) ? 1u : 0u) << (4 * q + 1);
+                msk |= (cand(x.z, fabsf(bf16_of(gw, 4 * q + 2)), byte_of(cw, 4 * q + 2), ct) ? 1u : 0u) << (4 * q + 2);
+                msk |= (cand(x.w, fabsf(bf16_of(gw, 4 * q + 3)), byte_of(cw, 4 * q + 3), ct) ? 1u : 0u) << (4 * q + 3);
             }
             while (msk) {
                 const int e = __ffs(msk) - 1;
@@ -633,30 +690,32 @@ step_kernel_thread(const StepArgs a) {
         const StateParams pm = state_params(md.x, md.y, tab);
         const StateParams pv = state_params(md.z, md.w, tab);
         const float eps_m = fast_err(pm.rkd.hi), eps_v = fast_err(pv.rkd.hi);
-        float fmx_m = 0.0f, fmx_v = 0.0f, gmx = 0.0f;
-        uint32_t fmn_m = 0xFFFFFFFEu, fmn_v = 0xFFFFFFFEu;
+        float fmx_m = 0.0f, fmx_v = 0.0f, gmx = 0.0f, fmn_m = kInf, fmn_v = kInf;
 #pragma unroll
         for (int i = 0; i < G; ++i) {
             const int e = j * G + i;
             const float gf = bf16_of(c.g, e);
-            fast_elem(a, byte_of(c.mq, e), byte_of(c.vq, e), gf, c.w[e], lg_hi, pm.P, pm.rkd.hi,
-                      pv.P, pv.rkd.hi, m[e], v[e]);
+            fast_elem<0>(a, byte_of(c.mq, e), byte_of(c.vq, e), gf, c.w[e], lg_hi, a.beta1 * pm.P,
+                         pm.rkd.hi, a.beta2 * pv.P, pv.rkd.hi, m[e], v[e]);
             fmx_m = fmaxf(fmx_m, fabsf(m[e]));
             fmx_v = fmaxf(fmx_v, v[e]);
             gmx = fmaxf(gmx, fabsf(gf));
-            fmn_m = min(fmn_m, min_key(m[e]));
-            fmn_v = min(fmn_v, min_key(v[e]));
+            fmn_m = fminf(fmn_m, nz_key(m[e]));
+            fmn_v = fminf(fmn_v, nz_key(v[e]));
         }
-        const GroupWin win = make_win(a, pm.P, eps_m, eps_v, fmx_m, min_key_value(fmn_m), fmx_v,
-                                      min_key_value(fmn_v), gmx);
+        const GroupWin win = make_win(a, pm.P, eps_m, eps_v, fmx_m, nz_key_value(fmn_m), fmx_v,
+                                      nz_key_value(fmn_v), gmx);
         float ex[4] = {0.0f, kInf, 0.0f, kInf};
         // every element inside any window is re-evaluated once and encoded exactly
 #pragma unroll
         for (int i = 0; i < G; ++i) {
             const int e = j * G + i;
             const float gf = bf16_of(c.g, e);
-            const bool cm = cand(m[e], fabsf(gf), 0, win, a.omb1) || cand(m[e], fabsf(gf), 1, win, a.omb1);
-            const bool cv = cand(v[e], 0.0f, 2, win, a.omb1) || cand(v[e], 0.0f, 3, win, a.omb1);
+            const uint32_t cmq = byte_of(c.mq, e), cvq = byte_of(c.vq, e);
+            const bool cm = cand(m[e], fabsf(gf), cmq, cand_test(win, 0, a.omb1)) ||
+                            cand(m[e], fabsf(gf), cmq, cand_test(win, 1, a.omb1));
+            const bool cv = cand(v[e], fabsf(gf), cvq, cand_test(win, 2, a.omb1)) ||
+                            cand(v[e], fabsf(gf), cvq, cand_test(win, 3, a.omb1));
             if (cm) {
                 m[e] = exact_moment(byte_of(c.mq, e), gf, false, pm.A, pm.rkd, pm.S, a.beta1,
                                     a.omb1, tab, lg_hi, lg_lo);
@@ -712,14 +771,15 @@ step_kernel_thread(const StepArgs a) {
 template <int G>
 cudaError_t launch_step(const StepArgs& a, cudaStream_t stream) {
     if constexpr (G >= kVec) {
-        using Lay = CtaLayout<G>;
+        constexpr int CTA = kStepCta;
+        using Lay = CtaLayout<G, CTA>;
         // more than 48 KB of dynamic shared memory needs the opt-in attribute
-        const cudaError_t e = cudaFuncSetAttribute(step_kernel_cta<G>,
+        const cudaError_t e = cudaFuncSetAttribute(step_kernel_cta<G, CTA>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)Lay::bytes);
         if (e != cudaSuccess) return e;
-        const int64_t blocks = (a.n + kCtaElems - 1) / kCtaElems;
-        step_kernel_cta<G><<<(unsigned)blocks, kCta, Lay::bytes, stream>>>(a);
+        const int64_t blocks = (a.n + Lay::kCtaElems - 1) / Lay::kCtaElems;
+        step_kernel_cta<G, CTA><<<(unsigned)blocks, CTA, Lay::bytes, stream>>>(a);
     } else {
         const int64_t threads = (a.n + kVec - 1) / kVec;
         const int64_t blocks = (threads + kThreadCta - 1) / kThreadCta;
