@@ -54,7 +54,7 @@ using df::F2;
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 #ifndef COAT_STEP_CTA
-#define COAT_STEP_CTA 256
+#define COAT_STEP_CTA 128
 #endif
 constexpr int kStepCta = COAT_STEP_CTA;    // threads per CTA of the cooperative kernel
 #define kInf __int_as_float(0x7F800000)
