@@ -19,17 +19,23 @@ from typing import Optional
 from . import _build
 
 __all__ = ["CoatError", "coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
-           "coat_fp8_adamw_step_host_workspace_bytes", "coat_dre_quantize", "coat_dre_dequantize",
-           "coat_status_string", "coat_r_e4m3", "coat_version", "lib", "lib_path",
-           "num_groups", "bytes_per_param", "STATUS"]
+           "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
+           "coat_dre_quantize", "coat_dre_dequantize", "coat_status_string", "coat_r_e4m3",
+           "coat_version", "lib", "lib_path", "num_groups", "bytes_per_param", "STATUS",
+           "STATIC_SCRATCH_BYTES"]
 
 STATUS = {0: "COAT_OK", 1: "COAT_ERR_INVALID_ARG", 2: "COAT_ERR_MISALIGNED",
-          3: "COAT_ERR_UNSUPPORTED_G", 4: "COAT_ERR_CUDA", 5: "COAT_ERR_NOT_DEVICE"}
+          3: "COAT_ERR_UNSUPPORTED_G", 4: "COAT_ERR_CUDA", 5: "COAT_ERR_NOT_DEVICE",
+          6: "COAT_ERR_SCRATCH_LIMIT"}
+
+#: COAT_STATIC_SCRATCH_BYTES of include/coat.h
+STATIC_SCRATCH_BYTES = 16 << 20
 
 #: symbols the shared library must export (one per declaration in include/coat.h)
 EXPORTS = ("coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
-           "coat_fp8_adamw_step_host_workspace_bytes", "coat_dre_quantize", "coat_dre_dequantize",
-           "coat_status_string", "coat_r_e4m3", "coat_version")
+           "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
+           "coat_dre_quantize", "coat_dre_dequantize", "coat_status_string", "coat_r_e4m3",
+           "coat_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +73,9 @@ def lib() -> ctypes.CDLL:
         L.coat_fp8_adamw_step_host.restype = ctypes.c_int
         L.coat_fp8_adamw_step_host_workspace_bytes.argtypes = [i64, i32]
         L.coat_fp8_adamw_step_host_workspace_bytes.restype = ctypes.c_size_t
+        L.coat_fp8_adamw_step_host_static.argtypes = [vp, vp, vp, vp, vp, i64, i32, f32, f32, f32,
+                                                      f32, f32, i64, i64, vp]
+        L.coat_fp8_adamw_step_host_static.restype = ctypes.c_int
         L.coat_dre_quantize.argtypes = [vp, i64, i32, vp, vp, vp, vp]
         L.coat_dre_quantize.restype = ctypes.c_int
         L.coat_dre_dequantize.argtypes = [vp, vp, vp, i64, i32, vp, vp]
@@ -192,6 +201,28 @@ def coat_fp8_adamw_step_host(w, g, m_q, v_q, meta, G: int, beta1: float, beta2: 
                                         _stream_ptr(stream))
     if st != 0:
         raise CoatError(st, "coat_fp8_adamw_step_host")
+
+
+def coat_fp8_adamw_step_host_static(w, g, m_q, v_q, meta, G: int, beta1: float, beta2: float,
+                                    lr: float, eps: float, weight_decay: float, step: int,
+                                    chunk_params: int = 0, stream=None) -> None:
+    """The step on host CPU tensors through the library's fixed device scratch
+    (COAT_STATIC_SCRATCH_BYTES): no device allocation, for callers that cannot
+    allocate.  Calls on one device must not overlap in time.  Returns when the
+    host tensors hold the result."""
+    import torch
+    n = w.numel()
+    pw = _check_host(w, torch.float32, n, "w")
+    pg = _check_host(g, torch.bfloat16, n, "g")
+    pm = _check_host(m_q, torch.uint8, n, "m_q")
+    pv = _check_host(v_q, torch.uint8, n, "v_q")
+    pmeta = _check_host(meta, torch.float32, 4 * num_groups(n, G), "meta")
+    st = lib().coat_fp8_adamw_step_host_static(pw, pg, pm, pv, pmeta, n, int(G), float(beta1),
+                                               float(beta2), float(lr), float(eps),
+                                               float(weight_decay), int(step), int(chunk_params),
+                                               _stream_ptr(stream))
+    if st != 0:
+        raise CoatError(st, "coat_fp8_adamw_step_host_static")
 
 
 def coat_dre_quantize(x, G: int, q, scale, k, stream=None) -> None:

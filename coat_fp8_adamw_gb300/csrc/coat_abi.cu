@@ -148,6 +148,7 @@ const char* coat_status_string(coat_status s) {
         case COAT_ERR_UNSUPPORTED_G: return "group size must be a power of two in [1, 256]";
         case COAT_ERR_CUDA: return "CUDA launch or runtime error";
         case COAT_ERR_NOT_DEVICE: return "pointer is not device memory";
+        case COAT_ERR_SCRATCH_LIMIT: return "request exceeds the library's static scratch";
     }
     return "unknown status";
 }

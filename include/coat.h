@@ -33,14 +33,15 @@
  * Conventions for every entry point below:
  *   - Data pointers are DEVICE pointers (cudaMalloc / torch CUDA tensors) on
  *     the current device, 16-byte aligned -- except the state buffers of
- *     coat_fp8_adamw_step_host, which are host pointers.  The library
- *     allocates no memory and keeps no state between calls
- *     (coat_fp8_adamw_step_host creates and destroys its three streams and
- *     one event within the call).
+ *     coat_fp8_adamw_step_host and coat_fp8_adamw_step_host_static, which
+ *     are host pointers.  The library allocates no memory and keeps no state
+ *     between calls (coat_fp8_adamw_step_host creates and destroys its three
+ *     streams and one event within the call; coat_fp8_adamw_step_host_static
+ *     keeps its scratch's device address per device).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call is asynchronous on that stream, except
- *     coat_fp8_adamw_step_host, which returns when its result is in host
- *     memory.
+ *     coat_fp8_adamw_step_host and coat_fp8_adamw_step_host_static, which
+ *     return when their result is in host memory.
  *   - G must be a power of two in [1, 256]; n >= 1.
  *   - Argument errors return a status and launch nothing.  A failed launch
  *     returns COAT_ERR_CUDA (the CUDA error is left for the caller to query
@@ -64,8 +65,12 @@ typedef enum {
     COAT_ERR_MISALIGNED = 2,    /* a pointer is not 16-byte aligned */
     COAT_ERR_UNSUPPORTED_G = 3, /* G not a power of two in [1, 256] */
     COAT_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
-    COAT_ERR_NOT_DEVICE = 5     /* a pointer is not device (or managed) memory */
+    COAT_ERR_NOT_DEVICE = 5,    /* a pointer is not device (or managed) memory */
+    COAT_ERR_SCRATCH_LIMIT = 6  /* the request needs more than COAT_STATIC_SCRATCH_BYTES */
 } coat_status;
+
+/* Size of the fixed device scratch buffer of coat_fp8_adamw_step_host_static. */
+#define COAT_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 
 /* Per-group record of the quantized optimizer state: 16 bytes, one per group,
  * scale and exponent of the first moment, then of the second moment. */
@@ -125,6 +130,52 @@ coat_status coat_fp8_adamw_step_host(float *w, const uint16_t *g, uint8_t *m_q, 
 /* Workspace bytes coat_fp8_adamw_step_host needs to stream chunks of
  * `chunk_params` parameters (rounded up to a multiple of 4096); 0 for a bad G. */
 size_t coat_fp8_adamw_step_host_workspace_bytes(int64_t chunk_params, int32_t G);
+
+/*
+ * coat_fp8_adamw_step_host for callers that cannot allocate device memory.
+ * The COAT review page has no counterpart: this entry point serves how the
+ * library is deployed, not the method.
+ *
+ * Who needs it: a process whose caching allocator already holds the device
+ * memory it may use (a workspace allocation would fail or fragment it), code
+ * that must not call cudaMalloc / cudaFree between steps (both can
+ * synchronize the whole device), and runtimes whose device footprint is fixed
+ * at start-up.  Instead of a caller's workspace, the step streams the state
+ * through a scratch buffer of COAT_STATIC_SCRATCH_BYTES (16 MiB) that is a
+ * file-scope __device__ array of the library: the CUDA runtime reserves it on
+ * a device when the library's module that holds it is loaded there.  The
+ * call allocates no memory (no cudaMalloc, no allocating library routine)
+ * and creates no stream or event.
+ *
+ * Everything runs on `stream`, one chunk after another: host->device copies,
+ * the step kernel, device->host copies.  Copies and compute do not overlap;
+ * where a workspace can be allocated, coat_fp8_adamw_step_host is faster.  The
+ * call returns once the host buffers hold the result, which is bit-identical
+ * to coat_fp8_adamw_step on device copies of the same buffers.
+ *
+ *   w, g, m_q, v_q, meta, n, G, beta1, beta2, lr, eps, weight_decay, step:
+ *                 as for coat_fp8_adamw_step_host (host pointers).
+ *   chunk_params  parameters per chunk, rounded up to a multiple of 4096;
+ *                 0 = the largest chunk that fits the scratch (about 2.06
+ *                 million parameters at G = 128, about 0.7 million at G = 1).
+ *
+ * Set-up: the first call on a device, made with that device current, looks
+ * up the scratch's device address (cudaGetSymbolAddress), which may load the
+ * module on that device; make that first call before any stream capture
+ * begins.  Nothing in the scratch has to start at zero: each chunk's bytes
+ * are copied in by the same call before the kernel reads them.
+ * One scratch per device: calls that overlap in time on one device (from
+ * several host threads, or on several streams) race on it; the caller must
+ * serialize them.
+ * Errors: COAT_ERR_SCRATCH_LIMIT when one chunk of chunk_params parameters
+ * needs more than COAT_STATIC_SCRATCH_BYTES (nothing is copied or launched);
+ * otherwise as coat_fp8_adamw_step_host.
+ */
+coat_status coat_fp8_adamw_step_host_static(float *w, const uint16_t *g, uint8_t *m_q,
+                                            uint8_t *v_q, coat_group_meta *meta, int64_t n,
+                                            int32_t G, float beta1, float beta2, float lr,
+                                            float eps, float weight_decay, int64_t step,
+                                            int64_t chunk_params, void *stream);
 
 /*
  * DRE + E4M3 quantization of one fp32 tensor (COAT review page, section 3,

@@ -81,3 +81,22 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(coat._build, "lib_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         coat.lib()
+
+
+def _static(L, chunk=0, w=A, g=A + 0x100000, mq=A + 0x200000, vq=A + 0x300000, meta=A + 0x400000,
+            n=256, G=128, step=1):
+    return L.coat_fp8_adamw_step_host_static(w, g, mq, vq, meta, n, G, 0.9, 0.95, 1e-4, 1e-8, 0.1,
+                                             step, chunk, None)
+
+
+def test_static_scratch_limits(L):
+    """Requests beyond the static scratch are refused before any pointer is used."""
+    assert _static(L, chunk=-1) == 1
+    assert _static(L, n=0) == 1
+    assert _static(L, G=3) == 3
+    assert _static(L, chunk=coat.STATIC_SCRATCH_BYTES + 1) == 6
+    assert _static(L, chunk=1 << 62) == 6
+    # one chunk of c parameters needs 8c bytes plus 16 per group, each part rounded to 256
+    assert _static(L, chunk=2_100_000) == 6
+    assert _static(L, G=1, chunk=700_000) == 6
+    assert coat.coat_status_string(6) == "request exceeds the library's static scratch"
