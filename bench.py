@@ -285,6 +285,8 @@ def run_ours(args):
     clocks.start()
     time.sleep(0.3)
     barrier()
+    # the timed region is the profiler's capture range (ncu --profile-from-start off)
+    torch.cuda.profiler.start()
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_begin.record(stream)
@@ -295,6 +297,7 @@ def run_ours(args):
         ends[i].record(stream)
     t_end.record(stream)
     barrier()
+    torch.cuda.profiler.stop()
     clk = clocks.stop()
     total_ms = t_begin.elapsed_time(t_end)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -369,10 +372,12 @@ def e2e_leg(args, coat, synth, torch, dev, w, g, mq, vq, meta, n, G, ng, hp, t):
                                       hp["lr"], hp["eps"], hp["weight_decay"], step_t, ws)
 
     one_step(t + 1)  # warm-up
+    torch.cuda.profiler.start()
     t0 = time.perf_counter()
     for i in range(args.e2e_steps):
         one_step(t + 2 + i)
     el = time.perf_counter() - t0
+    torch.cuda.profiler.stop()
     h2d = n * (4 + 2 + 1 + 1) + ng * 16
     d2h = n * (4 + 1 + 1) + ng * 16
     return {"value": n * args.e2e_steps / el, "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -88,12 +88,14 @@ __device__ __forceinline__ void load_chunk(const StepArgs& a, int64_t base, bool
             c.w[4 * i + 2] = v.z;
             c.w[4 * i + 3] = v.w;
         }
+        // g and the codes keep the default cache policy (not evict-first): the
+        // exact pass of this CTA reads some of them again a few microseconds later
         const uint4* gp = reinterpret_cast<const uint4*>(a.g + base);
-        const uint4 g0 = ld_cs(gp), g1 = ld_cs(gp + 1);
+        const uint4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
         c.g[0] = g0.x; c.g[1] = g0.y; c.g[2] = g0.z; c.g[3] = g0.w;
         c.g[4] = g1.x; c.g[5] = g1.y; c.g[6] = g1.z; c.g[7] = g1.w;
-        const uint4 m = ld_cs(reinterpret_cast<const uint4*>(a.mq + base));
-        const uint4 v = ld_cs(reinterpret_cast<const uint4*>(a.vq + base));
+        const uint4 m = __ldcg(reinterpret_cast<const uint4*>(a.mq + base));
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.vq + base));
         c.mq[0] = m.x; c.mq[1] = m.y; c.mq[2] = m.z; c.mq[3] = m.w;
         c.vq[0] = v.x; c.vq[1] = v.y; c.vq[2] = v.z; c.vq[3] = v.w;
     } else {
