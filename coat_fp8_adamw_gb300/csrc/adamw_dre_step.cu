@@ -440,9 +440,9 @@ step_kernel_cta(const StepArgs a) {
     if (active) load_chunk(a, base, full, c);
     else zero_chunk(c);
 
-    if (tid < 128) {
-        lg_hi[tid] = __uint_as_float(kLog2Frac448Hi[tid]);
-        lg_lo[tid] = __uint_as_float(kLog2Frac448Lo[tid]);
+    for (int i = tid; i < 128; i += kCta) {
+        lg_hi[i] = __uint_as_float(kLog2Frac448Hi[i]);
+        lg_lo[i] = __uint_as_float(kLog2Frac448Lo[i]);
     }
     load_smem_tables(st, tid, kCta);
     __syncthreads();
@@ -668,9 +668,9 @@ step_kernel_thread(const StepArgs a) {
     constexpr int NG = kVec / G;
     __shared__ float lg_hi[128], lg_lo[128];
     __shared__ SmemTables st;
-    if (threadIdx.x < 128) {
-        lg_hi[threadIdx.x] = __uint_as_float(kLog2Frac448Hi[threadIdx.x]);
-        lg_lo[threadIdx.x] = __uint_as_float(kLog2Frac448Lo[threadIdx.x]);
+    for (int i = threadIdx.x; i < 128; i += kThreadCta) {
+        lg_hi[i] = __uint_as_float(kLog2Frac448Hi[i]);
+        lg_lo[i] = __uint_as_float(kLog2Frac448Lo[i]);
     }
     load_smem_tables(st, threadIdx.x, kThreadCta);
     __syncthreads();

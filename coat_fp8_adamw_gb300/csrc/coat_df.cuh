@@ -196,8 +196,11 @@ COAT_HD F2 log2_df(float x, const Tables& t) {
 COAT_HD float exp2_df(F2 z, const Tables& t) {
     const float n = rint(z.hi);
     const F2 f = two_sum(sub(z.hi, n), z.lo);      // |f| <= 0.5 + tiny
-    const float jf = rint(mul(f.hi, 32.0f));       // -16..16
-    const int j = (int)jf;
+    const float jf = rint(mul(f.hi, 32.0f));       // -16..16 for a normalized z
+    // clamped so that no input (even a non-normalized or non-finite one) can
+    // index outside the 33-entry table
+    const int j0 = (int)jf;
+    const int j = j0 < -16 ? -16 : (j0 > 16 ? 16 : j0);
     const F2 r = fast_two_sum(sub(f.hi, mul(jf, 0.03125f)), f.lo);  // |r| <= 1/64
     // a = r ln 2
     const F2 a = mul22(r, F2{kLn2Hi, kLn2Lo});

@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kThreads)
 dre_dequantize_kernel(const DequantArgs a) {
     using Gm = Geom<G>;
     __shared__ float s_log[128];
-    if (threadIdx.x < 128) s_log[threadIdx.x] = __uint_as_float(kLog2Frac448Hi[threadIdx.x]);
+    for (int i = threadIdx.x; i < 128; i += kThreads) s_log[i] = __uint_as_float(kLog2Frac448Hi[i]);
     __syncthreads();
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t base = tid * kVec;
