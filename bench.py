@@ -32,6 +32,7 @@ METRIC = "FP8 AdamW+DRE step: params/s and achieved HBM GB/s (% of GB300 peak), 
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL = "step_kernel_cta"
+L2_BYTES = 129 * 2 ** 20
 
 
 def parse():
@@ -234,6 +235,19 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
+def quantile(xs, q: float) -> float:
+    """Nearest-rank quantile of a list of launch times."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, int(round(q * (len(ys) - 1)))))]
+
+
+def l2_note(working_set_bytes: float) -> str:
+    if working_set_bytes > 10 * L2_BYTES:
+        return "working set %.1f GB >> 129 MB L2: no flush needed" % (working_set_bytes / 1e9)
+    return ("working set %.2f GB is comparable to the 129 MB L2: timings are L2-affected "
+            "(a parity case, not a bench configuration)" % (working_set_bytes / 1e9))
+
+
 def run_ours(args):
     import torch
 
@@ -326,13 +340,15 @@ def run_ours(args):
                 "config": {"workload": f"{args.workload}-shaped parameter set", "G": G,
                            "params": n, "groups": ng, "bytes_per_param": bpp,
                            "parallelism": "replicas" if ws > 1 else "single GPU",
-                           "l2": "working set %.1f GB >> 129 MB L2: no flush needed"
-                                 % (bpp * n / 1e9)},
+                           "l2": l2_note(bpp * n)},
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
                              "unit": "GB/s", "frac": achieved / peak,
                              "peak_kind": f"{peak_kind} (copy bandwidth)",
                              "traffic": (traffic_bpp * n) if traffic_bpp else None,
                              "kernel": KERNEL, "avg_launch_ms": avg_launch,
+                             "median_launch_ms": statistics.median(launch_ms),
+                             "p10_launch_ms": quantile(launch_ms, 0.1),
+                             "p90_launch_ms": quantile(launch_ms, 0.9),
                              "min_launch_ms": min(launch_ms), "max_launch_ms": max(launch_ms)},
                 "gpu_launches": args.steps,
                 "clocks": clk,
