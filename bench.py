@@ -47,6 +47,11 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--report", default=None, choices=["dre-mse"],
+                   help="dre-mse: quantization error with and without the expansion on "
+                        "AdamW-like moments, and the codec kernels' bandwidth (one GPU)")
+    p.add_argument("--params", type=int, default=1 << 30,
+                   help="parameters of the dre-mse report")
     return p.parse_args()
 
 
@@ -402,8 +407,79 @@ def e2e_leg(args, coat, synth, torch, dev, w, g, mq, vq, meta, n, G, ng, hp, t):
                     "memory), host wall clock per call"}
 
 
+def report_dre_mse(args):
+    """Quantization MSE of AdamW-like first and second moments stored as E4M3
+    codes with and without Dynamic Range Expansion (the section 4 table of the
+    COAT review page credits the expansion with a 1.63x lower MSE), plus the
+    achieved bandwidth of the three codec kernels.  Everything runs on the GPU
+    through the C ABI; the oracle cross-checks the same numbers in the tests."""
+    import torch
+
+    import coat_fp8_adamw_gb300 as coat
+    from coat_fp8_adamw_gb300 import synth
+    coat.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n, G = args.params, args.G
+    ng = coat.num_groups(n, G)
+    stream = torch.cuda.current_stream()
+    out = {"report": "dre-mse", "params": n, "G": G, "data": "synthetic AdamW-like moments",
+           "moments": {}, "kernels": {}}
+    peak, peak_kind = measured_peak()
+    q = torch.empty(n, dtype=torch.uint8, device=dev)
+    S = torch.empty(ng, dtype=torch.float32, device=dev)
+    k = torch.empty(ng, dtype=torch.float32, device=dev)
+    ones = torch.ones(ng, dtype=torch.float32, device=dev)
+    back = torch.empty(n, dtype=torch.float32, device=dev)
+
+    def timed(fn, bytes_moved):
+        for _ in range(3):
+            fn()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        reps = 10
+        for _ in range(reps):
+            fn()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        ms = ev[0].elapsed_time(ev[1]) / reps
+        gbs = bytes_moved / (ms / 1e3) / 1e9
+        return {"ms": ms, "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak,
+                "peak_kind": peak_kind}
+
+    m, v = synth.adamw_like_moments_torch(n, G, 11, dev)
+    for name, x in (("m", m), ("v", v)):
+        xd = x.double()
+        norm = float((xd * xd).mean())
+        coat.coat_dre_quantize(x, G, q, S, k)
+        coat.coat_dre_dequantize(q, S, k, G, back)
+        mse_dre = float(((back.double() - xd) ** 2).mean())
+        kk = k.double()
+        coat.coat_fp8_quantize_absmax(x, G, q, S)
+        coat.coat_dre_dequantize(q, S, ones, G, back)
+        mse_abs = float(((back.double() - xd) ** 2).mean())
+        out["moments"][name] = {"mse_dre": mse_dre, "mse_no_dre": mse_abs,
+                                "relative_mse_dre": mse_dre / norm,
+                                "relative_mse_no_dre": mse_abs / norm,
+                                "no_dre_over_dre": mse_abs / mse_dre,
+                                "k_median": float(kk.median()), "k_p10": float(kk.quantile(0.1)),
+                                "k_p90": float(kk.quantile(0.9))}
+    x = v
+    out["kernels"]["dre_quantize"] = timed(lambda: coat.coat_dre_quantize(x, G, q, S, k),
+                                           n * 5 + ng * 8)
+    out["kernels"]["fp8_quantize_absmax"] = timed(lambda: coat.coat_fp8_quantize_absmax(x, G, q, S),
+                                                  n * 5 + ng * 4)
+    out["kernels"]["dre_dequantize"] = timed(lambda: coat.coat_dre_dequantize(q, S, k, G, back),
+                                             n * 5 + ng * 8)
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
+    if args.report == "dre-mse":
+        report_dre_mse(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -20,8 +20,9 @@ from . import _build
 
 __all__ = ["CoatError", "coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
            "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
-           "coat_dre_quantize", "coat_dre_dequantize", "coat_status_string", "coat_r_e4m3",
-           "coat_version", "lib", "lib_path", "num_groups", "bytes_per_param", "STATUS",
+           "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_dre_dequantize",
+           "coat_status_string", "coat_r_e4m3", "coat_version", "lib", "lib_path", "num_groups",
+           "bytes_per_param", "STATUS",
            "STATIC_SCRATCH_BYTES"]
 
 STATUS = {0: "COAT_OK", 1: "COAT_ERR_INVALID_ARG", 2: "COAT_ERR_MISALIGNED",
@@ -34,8 +35,8 @@ STATIC_SCRATCH_BYTES = 16 << 20
 #: symbols the shared library must export (one per declaration in include/coat.h)
 EXPORTS = ("coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
            "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
-           "coat_dre_quantize", "coat_dre_dequantize", "coat_status_string", "coat_r_e4m3",
-           "coat_version")
+           "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_dre_dequantize",
+           "coat_status_string", "coat_r_e4m3", "coat_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.coat_fp8_adamw_step_host_static.restype = ctypes.c_int
         L.coat_dre_quantize.argtypes = [vp, i64, i32, vp, vp, vp, vp]
         L.coat_dre_quantize.restype = ctypes.c_int
+        L.coat_fp8_quantize_absmax.argtypes = [vp, i64, i32, vp, vp, vp]
+        L.coat_fp8_quantize_absmax.restype = ctypes.c_int
         L.coat_dre_dequantize.argtypes = [vp, vp, vp, i64, i32, vp, vp]
         L.coat_dre_dequantize.restype = ctypes.c_int
         L.coat_status_string.argtypes = [ctypes.c_int]
@@ -237,6 +240,20 @@ def coat_dre_quantize(x, G: int, q, scale, k, stream=None) -> None:
     st = lib().coat_dre_quantize(px, n, int(G), pq, ps, pk, _stream_ptr(stream))
     if st != 0:
         raise CoatError(st, "coat_dre_quantize")
+
+
+def coat_fp8_quantize_absmax(x, G: int, q, scale, stream=None) -> None:
+    """Per-group FP8 without the expansion: x fp32 [n] -> q uint8 [n], scale fp32 [ceil(n/G)]
+    (scale = max|x| / 448; decode with coat_dre_dequantize and k = 1)."""
+    import torch
+    n = x.numel()
+    ng = num_groups(n, G)
+    px = _check(x, torch.float32, n, "x")
+    pq = _check(q, torch.uint8, n, "q", x.device)
+    ps = _check(scale, torch.float32, ng, "scale", x.device)
+    st = lib().coat_fp8_quantize_absmax(px, n, int(G), pq, ps, _stream_ptr(stream))
+    if st != 0:
+        raise CoatError(st, "coat_fp8_quantize_absmax")
 
 
 def coat_dre_dequantize(q, scale, k, G: int, x, stream=None) -> None:

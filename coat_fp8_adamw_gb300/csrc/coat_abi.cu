@@ -124,6 +124,20 @@ coat_status coat_dre_quantize(const float* x, int64_t n, int32_t G, uint8_t* q, 
     return from_cuda(coat::launch_dre_quantize(a, G, static_cast<cudaStream_t>(stream)));
 }
 
+coat_status coat_fp8_quantize_absmax(const float* x, int64_t n, int32_t G, uint8_t* q, float* scale,
+                                     void* stream) {
+    if (!x || !q || !scale || n < 1) return COAT_ERR_INVALID_ARG;
+    if (!pow2_group(G)) return COAT_ERR_UNSUPPORTED_G;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scale)) return COAT_ERR_MISALIGNED;
+    const size_t nb = (size_t)n, ng = (size_t)num_groups(n, G);
+    if (overlaps(x, 4 * nb, q, nb) || overlaps(x, 4 * nb, scale, 4 * ng) ||
+        overlaps(q, nb, scale, 4 * ng))
+        return COAT_ERR_INVALID_ARG;
+    if (!is_device(x) || !is_device(q) || !is_device(scale)) return COAT_ERR_NOT_DEVICE;
+    coat::QuantArgs a{x, q, scale, nullptr, n};
+    return from_cuda(coat::launch_absmax_quantize(a, G, static_cast<cudaStream_t>(stream)));
+}
+
 coat_status coat_dre_dequantize(const uint8_t* q, const float* scale, const float* k, int64_t n,
                                 int32_t G, float* x, void* stream) {
     if (!x || !q || !scale || !k || n < 1) return COAT_ERR_INVALID_ARG;

@@ -55,6 +55,7 @@ coat_status check_step_args(const float* w, const uint16_t* g, const uint8_t* m_
 coat_status make_step_args(float beta1, float beta2, float lr, float eps, float weight_decay,
                            int64_t step, StepArgs& a);
 cudaError_t launch_dre_quantize(const QuantArgs& a, int G, cudaStream_t stream);
+cudaError_t launch_absmax_quantize(const QuantArgs& a, int G, cudaStream_t stream);
 cudaError_t launch_dre_dequantize(const DequantArgs& a, int G, cudaStream_t stream);
 
 }  // namespace coat

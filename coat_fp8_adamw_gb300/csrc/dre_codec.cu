@@ -146,6 +146,77 @@ dre_dequantize_kernel(const DequantArgs a) {
     }
 }
 
+// Plain per-group FP8 quantization without the expansion (section 3 FP8
+// quantization equation alone: S = max|X| / 448, q = RNE(X / S), saturating):
+// the reference point the expansion is measured against.
+template <int G>
+__global__ void __launch_bounds__(kThreads)
+absmax_quantize_kernel(const QuantArgs a) {
+    using Gm = Geom<G>;
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t base = tid * kVec;
+    if (__all_sync(0xFFFFFFFFu, base >= a.n)) return;
+    const bool active = base < a.n;
+    const bool full = base + kVec <= a.n;
+
+    float x[kVec];
+    if (active && full) {
+        const float4* xp = reinterpret_cast<const float4*>(a.x + base);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 t = ld_cs(xp + i);
+            x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) x[e] = (active && base + e < a.n) ? a.x[base + e] : 0.0f;
+    }
+    float mx[Gm::kGroups];
+#pragma unroll
+    for (int j = 0; j < Gm::kGroups; ++j) mx[j] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) mx[e / Gm::kElems] = fmaxf(mx[e / Gm::kElems], fabsf(x[e]));
+#pragma unroll
+    for (int off = Gm::kLanes / 2; off > 0; off >>= 1)
+        mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xFFFFFFFFu, mx[0], off));
+    float S[Gm::kGroups];
+#pragma unroll
+    for (int j = 0; j < Gm::kGroups; ++j) S[j] = __fdiv_rn(mx[j], 448.0f);
+    if (!active) return;
+
+    uint32_t out[kVec / 4];
+#pragma unroll
+    for (int e = 0; e < kVec; e += 2) {
+        const int j0 = e / Gm::kElems, j1 = (e + 1) / Gm::kElems;
+        // +0 for a zero (or an all-zero group): the code of a zero is 0x00
+        const float y0 = S[j0] > 0.0f ? __fadd_rn(__fdiv_rn(x[e], S[j0]), 0.0f) : 0.0f;
+        const float y1 = S[j1] > 0.0f ? __fadd_rn(__fdiv_rn(x[e + 1], S[j1]), 0.0f) : 0.0f;
+        const uint32_t p = e4m3x2(y0, y1);
+        if ((e & 2) == 0) out[e / 4] = p; else out[e / 4] |= p << 16;
+    }
+    if (full) {
+        st_cs(reinterpret_cast<uint4*>(a.q + base), make_uint4(out[0], out[1], out[2], out[3]));
+    } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e)
+            if (base + e < a.n) a.q[base + e] = (uint8_t)(out[e / 4] >> (8 * (e & 3)));
+    }
+    const int64_t g0 = base / G;
+    const bool leader = G >= kVec ? ((base % G) == 0) : true;
+    if (leader) {
+#pragma unroll
+        for (int j = 0; j < Gm::kGroups; ++j)
+            if ((g0 + j) * G < a.n) a.scale[g0 + j] = S[j];
+    }
+}
+
+template <int G>
+cudaError_t launch_absmax(const QuantArgs& a, cudaStream_t s) {
+    const int64_t threads = (a.n + kVec - 1) / kVec;
+    absmax_quantize_kernel<G><<<(unsigned)((threads + kThreads - 1) / kThreads), kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <int G>
 cudaError_t launch_q(const QuantArgs& a, cudaStream_t s) {
     const int64_t threads = (a.n + kVec - 1) / kVec;
@@ -161,6 +232,21 @@ cudaError_t launch_dq(const DequantArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_absmax_quantize(const QuantArgs& a, int G, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_absmax<1>(a, s);
+        case 2: return launch_absmax<2>(a, s);
+        case 4: return launch_absmax<4>(a, s);
+        case 8: return launch_absmax<8>(a, s);
+        case 16: return launch_absmax<16>(a, s);
+        case 32: return launch_absmax<32>(a, s);
+        case 64: return launch_absmax<64>(a, s);
+        case 128: return launch_absmax<128>(a, s);
+        case 256: return launch_absmax<256>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_dre_quantize(const QuantArgs& a, int G, cudaStream_t s) {
     switch (G) {

@@ -263,6 +263,34 @@ def random_state_torch(n: int, G: int, seed: int, device):
     return mq, vq, meta
 
 
+def adamw_like_moments_np(n: int, G: int, seed: int):
+    """fp32 first and second moments coupled like real AdamW moments.
+
+    Per group a gradient scale s is drawn log-uniform in [1e-6, 1e-2]; per
+    element s_e = s exp(0.5 z); then m ~ 0.23 s_e N(0, 1) (the spread of an
+    EMA with beta1 = 0.9 of i.i.d. gradients) and v ~ s_e^2 (0.5 + U[0, 1]).
+    """
+    rng = np.random.default_rng([seed, 31])
+    ng = (n + G - 1) // G
+    s = np.repeat(10.0 ** rng.uniform(-6, -2, ng), G)[:n]
+    se = s * np.exp(0.5 * rng.standard_normal(n))
+    m = (0.23 * se * rng.standard_normal(n)).astype(np.float32)
+    v = (se * se * (0.5 + rng.random(n))).astype(np.float32)
+    return m, v
+
+
+def adamw_like_moments_torch(n: int, G: int, seed: int, device):
+    """Device version of :func:`adamw_like_moments_np` (same distributions, torch RNG)."""
+    import torch
+    gen = _gen(device, seed * 7919 + 3)
+    ng = (n + G - 1) // G
+    s = torch.pow(10.0, torch.rand(ng, generator=gen, device=device) * 4.0 - 6.0)
+    se = s.repeat_interleave(G)[:n] * torch.exp(0.5 * torch.randn(n, generator=gen, device=device))
+    m = 0.23 * se * torch.randn(n, generator=gen, device=device)
+    v = se * se * (0.5 + torch.rand(n, generator=gen, device=device))
+    return m.float(), v.float()
+
+
 def sample_groups(num_groups: int, count: int, seed: int) -> np.ndarray:
     """Sorted sample of group indices: the first, the last and ``count`` random ones."""
     rng = np.random.default_rng([seed, 99])

@@ -187,6 +187,19 @@ coat_status coat_dre_quantize(const float *x, int64_t n, int32_t G, uint8_t *q, 
                               float *k, void *stream);
 
 /*
+ * Per-group FP8 quantization WITHOUT the expansion (COAT review page,
+ * section 3, the FP8 quantization equation alone): scale = max|X| / 448
+ * rounded to float, q = E4M3(X / scale) rounded to nearest even and saturating
+ * at +-448; an all-zero group gets scale 0 and zero codes.  It is the plain
+ * per-group FP8 storage that Dynamic Range Expansion is measured against
+ * (the section 4 table credits the expansion with a 1.63x lower quantization
+ * MSE).  Decode with coat_dre_dequantize and k = 1 for every group.
+ *   x [n] float32 in;  q [n] uint8 out;  scale [ceil(n/G)] float32 out.
+ */
+coat_status coat_fp8_quantize_absmax(const float *x, int64_t n, int32_t G, uint8_t *q,
+                                     float *scale, void *stream);
+
+/*
  * Inverse of coat_dre_quantize: x = sign(q) (|E4M3(q)| scale)^(1/k).
  *   q [n] uint8 in;  scale, k [ceil(n/G)] float32 in (k > 0);  x [n] float32 out.
  */

@@ -80,6 +80,8 @@ def _load():
         lib.coat_oracle_dre_quantize.argtypes = [c_f32p, i64, i32, f64, c_u8p, c_f32p, c_f32p,
                                                  ctypes.c_int]
         lib.coat_oracle_dre_quantize.restype = ctypes.c_int
+        lib.coat_oracle_absmax_quantize.argtypes = [c_f32p, i64, i32, c_u8p, c_f32p, ctypes.c_int]
+        lib.coat_oracle_absmax_quantize.restype = ctypes.c_int
         lib.coat_oracle_dre_dequantize.argtypes = [c_u8p, c_f32p, c_f32p, i64, i32, c_f32p,
                                                    ctypes.c_int]
         lib.coat_oracle_dre_dequantize.restype = ctypes.c_int
@@ -165,6 +167,23 @@ def dre_quantize(x: np.ndarray, G: int, R: float = R_E4M3_DEFAULT, nthreads: int
     if rc != 0:
         raise ValueError("oracle dre_quantize: bad arguments")
     return q, S, k
+
+
+def absmax_quantize(x: np.ndarray, G: int, nthreads: int = 0):
+    """Per-group FP8 quantization without the expansion -> (q, S): S = max|x| / 448
+    rounded to float, q = E4M3(x / S) (section 3, FP8 quantization equation)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    n = x.size
+    ng = (n + G - 1) // G
+    q = np.zeros(n, dtype=np.uint8)
+    S = np.zeros(ng, dtype=np.float32)
+    rc = lib.coat_oracle_absmax_quantize(_ptr(x, ctypes.c_float), n, int(G),
+                                         _ptr(q, ctypes.c_uint8), _ptr(S, ctypes.c_float),
+                                         int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle absmax_quantize: bad arguments")
+    return q, S
 
 
 def dre_dequantize(q: np.ndarray, S: np.ndarray, k: np.ndarray, G: int,

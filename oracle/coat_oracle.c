@@ -323,6 +323,45 @@ int coat_oracle_dre_quantize(const float *x, int64_t n, int32_t G, double R, uin
     return 0;
 }
 
+/* FP8 quantization without the expansion (section 3, the FP8 quantization
+ * equation alone): S = max|X| / 448 rounded to float, q = E4M3(X / S). */
+typedef struct {
+    const float *x;
+    int64_t n;
+    int32_t G;
+    uint8_t *q;
+    float *S;
+} absmax_ctx;
+
+static void absmax_groups(void *c, int64_t g0, int64_t g1)
+{
+    absmax_ctx *a = (absmax_ctx *)c;
+    for (int64_t g = g0; g < g1; ++g) {
+        int64_t b = g * a->G, e = b + a->G;
+        if (e > a->n)
+            e = a->n;
+        double mx = 0.0;
+        for (int64_t i = b; i < e; ++i)
+            if (fabs((double)a->x[i]) > mx)
+                mx = fabs((double)a->x[i]);
+        float S32 = (float)(mx / 448.0);
+        a->S[g] = S32;
+        for (int64_t i = b; i < e; ++i)
+            a->q[i] = (uint8_t)(S32 > 0.0f ? coat_oracle_e4m3_encode((double)a->x[i] / (double)S32)
+                                           : 0);
+    }
+}
+
+int coat_oracle_absmax_quantize(const float *x, int64_t n, int32_t G, uint8_t *q, float *S,
+                                int nthreads)
+{
+    if (n <= 0 || G <= 0 || !x || !q || !S)
+        return 1;
+    absmax_ctx c = {x, n, G, q, S};
+    run_groups(absmax_groups, &c, (n + G - 1) / G, nthreads);
+    return 0;
+}
+
 typedef struct {
     const uint8_t *q;
     const float *S;

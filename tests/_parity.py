@@ -96,12 +96,8 @@ def adamw_like_state(n: int, G: int, seed: int, oracle):
     second moment, an update no AdamW trajectory produces.
     """
     import numpy as np
-    rng = np.random.default_rng([seed, 31])
-    ng = (n + G - 1) // G
-    s = np.repeat(10.0 ** rng.uniform(-6, -2, ng), G)[:n]
-    se = s * np.exp(0.5 * rng.standard_normal(n))
-    m = (0.23 * se * rng.standard_normal(n)).astype(np.float32)
-    v = (se * se * (0.5 + rng.random(n))).astype(np.float32)
+    from coat_fp8_adamw_gb300 import synth
+    m, v = synth.adamw_like_moments_np(n, G, seed)
     mq, Sm, km = oracle.dre_quantize(m, G)
     vq, Sv, kv = oracle.dre_quantize(v, G)
     meta = np.stack([Sm, km, Sv, kv], axis=1).astype(np.float32)

@@ -100,3 +100,12 @@ def test_static_scratch_limits(L):
     assert _static(L, chunk=2_100_000) == 6
     assert _static(L, G=1, chunk=700_000) == 6
     assert coat.coat_status_string(6) == "request exceeds the library's static scratch"
+
+
+def test_absmax_quantizer_validation(L):
+    assert L.coat_fp8_quantize_absmax(0, 16, 16, A, A + 4096, None) == 1
+    assert L.coat_fp8_quantize_absmax(A, 0, 16, A + 4096, A + 8192, None) == 1
+    assert L.coat_fp8_quantize_absmax(A, 16, 12, A + 4096, A + 8192, None) == 3
+    assert L.coat_fp8_quantize_absmax(A + 4, 16, 16, A + 4096, A + 8192, None) == 2
+    assert L.coat_fp8_quantize_absmax(A, 64, 16, A + 16, A + 8192, None) == 1   # x overlaps q
+    assert L.coat_fp8_quantize_absmax(A, 64, 16, A + 4096, A + 8192, None) == 5
