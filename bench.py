@@ -47,9 +47,12 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
-    p.add_argument("--report", default=None, choices=["dre-mse"],
+    p.add_argument("--report", default=None, choices=["dre-mse", "act-quant"],
                    help="dre-mse: quantization error with and without the expansion on "
-                        "AdamW-like moments, and the codec kernels' bandwidth (one GPU)")
+                        "AdamW-like moments, and the codec kernels' bandwidth; act-quant: "
+                        "bandwidth of the per-group FP8 activation quantizer (one GPU)")
+    p.add_argument("--rows", type=int, default=32768, help="M of the act-quant report")
+    p.add_argument("--cols", type=int, default=8192, help="N of the act-quant report")
     p.add_argument("--params", type=int, default=1 << 30,
                    help="parameters of the dre-mse report")
     return p.parse_args()
@@ -475,10 +478,54 @@ def report_dre_mse(args):
     print(json.dumps(out), flush=True)
 
 
+def report_act_quant(args):
+    """Achieved HBM bandwidth of the per-group (1 x G) FP8 activation quantizer
+    with its transposed second output, over the group sizes of the section 5
+    table, on a synthetic bf16 activation of --rows x --cols."""
+    import torch
+
+    import coat_fp8_adamw_gb300 as coat
+    coat.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    M, N = args.rows, args.cols
+    gen = torch.Generator(device=dev).manual_seed(7)
+    x = torch.randn(M, N, generator=gen, device=dev)
+    x = (x * torch.pow(10.0, torch.rand(M, 1, generator=gen, device=dev) * 4 - 3)).to(torch.bfloat16)
+    q = torch.empty((M, N), dtype=torch.uint8, device=dev)
+    qt = torch.empty((N, M), dtype=torch.uint8, device=dev)
+    peak, peak_kind = measured_peak()
+    stream = torch.cuda.current_stream()
+    out = {"report": "act-quant", "rows": M, "cols": N, "data": "synthetic bf16 activation",
+           "dtype": "bf16 in, e4m3 out", "by_G": {}}
+    for G in (4, 8, 16, 32, 64, 128):
+        S = torch.empty((M, N // G), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            coat.coat_act_quantize_fp8(x, G, q, S, qt)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        reps = 10
+        for _ in range(reps):
+            coat.coat_act_quantize_fp8(x, G, q, S, qt)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        ms = ev[0].elapsed_time(ev[1]) / reps
+        bytes_moved = M * N * (2 + 1 + 1) + (M * N // G) * 4
+        gbs = bytes_moved / (ms / 1e3) / 1e9
+        out["by_G"][str(G)] = {"ms": ms, "elements_per_s": M * N / (ms / 1e3),
+                               "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak,
+                               "bytes_per_element": 4 + 4 / G, "peak_kind": peak_kind}
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     if args.report == "dre-mse":
         report_dre_mse(args)
+        return
+    if args.report == "act-quant":
+        report_act_quant(args)
         return
     if args.impl == "reference":
         run_reference(args)

@@ -20,9 +20,9 @@ from . import _build
 
 __all__ = ["CoatError", "coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
            "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
-           "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_dre_dequantize",
-           "coat_status_string", "coat_r_e4m3", "coat_version", "lib", "lib_path", "num_groups",
-           "bytes_per_param", "STATUS",
+           "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_act_quantize_fp8",
+           "coat_dre_dequantize", "coat_status_string", "coat_r_e4m3", "coat_version", "lib",
+           "lib_path", "num_groups", "bytes_per_param", "STATUS",
            "STATIC_SCRATCH_BYTES"]
 
 STATUS = {0: "COAT_OK", 1: "COAT_ERR_INVALID_ARG", 2: "COAT_ERR_MISALIGNED",
@@ -35,8 +35,8 @@ STATIC_SCRATCH_BYTES = 16 << 20
 #: symbols the shared library must export (one per declaration in include/coat.h)
 EXPORTS = ("coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
            "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
-           "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_dre_dequantize",
-           "coat_status_string", "coat_r_e4m3", "coat_version")
+           "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_act_quantize_fp8",
+           "coat_dre_dequantize", "coat_status_string", "coat_r_e4m3", "coat_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.coat_dre_quantize.restype = ctypes.c_int
         L.coat_fp8_quantize_absmax.argtypes = [vp, i64, i32, vp, vp, vp]
         L.coat_fp8_quantize_absmax.restype = ctypes.c_int
+        L.coat_act_quantize_fp8.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp]
+        L.coat_act_quantize_fp8.restype = ctypes.c_int
         L.coat_dre_dequantize.argtypes = [vp, vp, vp, i64, i32, vp, vp]
         L.coat_dre_dequantize.restype = ctypes.c_int
         L.coat_status_string.argtypes = [ctypes.c_int]
@@ -254,6 +256,22 @@ def coat_fp8_quantize_absmax(x, G: int, q, scale, stream=None) -> None:
     st = lib().coat_fp8_quantize_absmax(px, n, int(G), pq, ps, _stream_ptr(stream))
     if st != 0:
         raise CoatError(st, "coat_fp8_quantize_absmax")
+
+
+def coat_act_quantize_fp8(x, G: int, q, scale, qt=None, stream=None) -> None:
+    """Per-group (1 x G) FP8 quantization of a bf16 activation x [M, N]:
+    q uint8 [M, N], scale fp32 [M, N/G], and optionally qt uint8 [N, M] (the codes transposed)."""
+    import torch
+    if x.dim() != 2:
+        raise ValueError("x must be a 2-D [M, N] tensor")
+    M, N = x.shape
+    px = _check(x, torch.bfloat16, M * N, "x")
+    pq = _check(q, torch.uint8, M * N, "q", x.device)
+    ps = _check(scale, torch.float32, (M * N) // G if G > 0 else 0, "scale", x.device)
+    pqt = _check(qt, torch.uint8, M * N, "qt", x.device) if qt is not None else None
+    st = lib().coat_act_quantize_fp8(px, M, N, int(G), pq, pqt, ps, _stream_ptr(stream))
+    if st != 0:
+        raise CoatError(st, "coat_act_quantize_fp8")
 
 
 def coat_dre_dequantize(q, scale, k, G: int, x, stream=None) -> None:

@@ -1,0 +1,154 @@
+// act_quant.cu -- per-group (1 x G) FP8 quantization of an activation tensor
+// with a transposed FP8 second output (COAT review page, section 4,
+// "non-linear layer optimisation": quantized FP8 output plus a transposed FP8
+// output for the backward pass; groups along the last dimension with a
+// two-stage maximum reduction).
+//
+// x is an M x N bf16 tensor in row-major order.  Each row is split into
+// groups of G consecutive elements; a group's scale is S = max|x| / 448 and its
+// codes are E4M3(x / S), rounded to nearest even, saturating.  q holds the
+// codes in the layout of x (M x N); qt holds the same codes transposed (N x M),
+// so that the backward pass reads contiguous columns.
+//
+// A CTA owns a 64 x 128 tile: 128 threads quantize it row by row (8 elements
+// per thread and pass, statistics per thread and then across the G/8 lanes of
+// a group), store q and the scales, stage the codes in shared memory, and then
+// write qt as 16-byte runs of one column, each built from 4 x 4 byte
+// transposes.
+#include <cstdint>
+
+#include "coat_device.cuh"
+#include "coat_kernels.h"
+
+namespace coat {
+
+namespace {
+
+constexpr int kTileR = 64;                  // rows per tile
+constexpr int kTileC = 128;                 // columns per tile
+constexpr int kActThreads = 128;
+constexpr int kPitchW = kTileC / 4 + 1;     // shared-memory row pitch in words (padded)
+
+template <int G>
+__global__ void __launch_bounds__(kActThreads)
+act_quant_kernel(const ActArgs a) {
+    __shared__ uint32_t tile[kTileR * kPitchW];
+    const int tid = threadIdx.x;
+    const int64_t row0 = (int64_t)blockIdx.y * kTileR;
+    const int64_t col0 = (int64_t)blockIdx.x * kTileC;
+    const int64_t ngr = a.N / G;            // groups per row
+
+    // ---- quantize: pass p covers rows 8p .. 8p+7, 16 threads per row ----
+    const int r_in = tid >> 4;              // row within the pass
+    const int c8 = (tid & 15) * 8;          // first column of this thread
+    const bool col_ok = col0 + c8 < a.N;    // N % 16 == 0: all 8 columns or none
+    uint4 raw[kTileR / 8];
+#pragma unroll
+    for (int p = 0; p < kTileR / 8; ++p) {
+        const int64_t r = row0 + 8 * p + r_in;
+        raw[p] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < a.M && col_ok) raw[p] = ld_cs(reinterpret_cast<const uint4*>(a.x + r * a.N + col0 + c8));
+    }
+#pragma unroll
+    for (int p = 0; p < kTileR / 8; ++p) {
+        const int64_t r = row0 + 8 * p + r_in;
+        const uint32_t w[4] = {raw[p].x, raw[p].y, raw[p].z, raw[p].w};
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+        constexpr int kGroupsHere = G >= 8 ? 1 : 8 / G;   // groups in this thread's 8 elements
+        constexpr int kPer = G >= 8 ? 8 : G;               // elements of one group here
+        float S[kGroupsHere];
+#pragma unroll
+        for (int j = 0; j < kGroupsHere; ++j) {
+            float mx = 0.0f;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) mx = fmaxf(mx, fabsf(x[j * kPer + e]));
+            if constexpr (G > 8) {
+#pragma unroll
+                for (int off = G / 16; off > 0; off >>= 1)
+                    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+            }
+            S[j] = __fdiv_rn(mx, 448.0f);
+        }
+        uint32_t codes[2];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const float s0 = S[e / kPer], s1 = S[(e + 1) / kPer];
+            // +0 for a zero (or an all-zero group): the code of a zero is 0x00
+            const float y0 = s0 > 0.0f ? __fadd_rn(e4m3_quotient(x[e], s0), 0.0f) : 0.0f;
+            const float y1 = s1 > 0.0f ? __fadd_rn(e4m3_quotient(x[e + 1], s1), 0.0f) : 0.0f;
+            const uint32_t pr = e4m3x2(y0, y1);
+            if ((e & 2) == 0) codes[e / 4] = pr; else codes[e / 4] |= pr << 16;
+        }
+        const int tr = 8 * p + r_in;
+        tile[tr * kPitchW + c8 / 4] = codes[0];
+        tile[tr * kPitchW + c8 / 4 + 1] = codes[1];
+        if (r < a.M && col_ok) {
+            __stcs(reinterpret_cast<uint2*>(a.q + r * a.N + col0 + c8), make_uint2(codes[0], codes[1]));
+            const int64_t g = (col0 + c8) / G;
+            if constexpr (G >= 8) {
+                if ((c8 % G) == 0) a.scale[r * ngr + g] = S[0];
+            } else {
+#pragma unroll
+                for (int j = 0; j < kGroupsHere; ++j) a.scale[r * ngr + g + j] = S[j];
+            }
+        }
+    }
+    if (a.qt == nullptr) return;
+    __syncthreads();
+
+    // ---- transposed output: thread = (column quad, 16-row chunk) ----
+    const int cq = tid & 31;                // columns 4 cq .. 4 cq + 3
+    const int rc = tid >> 5;                // rows 16 rc .. 16 rc + 15
+    const int64_t c_first = col0 + 4 * cq;
+    const int64_t r_first = row0 + 16 * rc;
+    if (c_first >= a.N || r_first >= a.M) return;   // N, M % 16 == 0: whole quads and chunks
+    uint32_t col[4][4];                     // [column j][block b]: rows 4b .. 4b+3
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int tr = 16 * rc + 4 * b;
+        const uint32_t w0 = tile[(tr + 0) * kPitchW + cq];
+        const uint32_t w1 = tile[(tr + 1) * kPitchW + cq];
+        const uint32_t w2 = tile[(tr + 2) * kPitchW + cq];
+        const uint32_t w3 = tile[(tr + 3) * kPitchW + cq];
+        const uint32_t t0 = __byte_perm(w0, w1, 0x5140);   // w0.b0 w1.b0 w0.b1 w1.b1
+        const uint32_t t1 = __byte_perm(w2, w3, 0x5140);
+        const uint32_t t2 = __byte_perm(w0, w1, 0x7362);   // w0.b2 w1.b2 w0.b3 w1.b3
+        const uint32_t t3 = __byte_perm(w2, w3, 0x7362);
+        col[0][b] = __byte_perm(t0, t1, 0x5410);
+        col[1][b] = __byte_perm(t0, t1, 0x7632);
+        col[2][b] = __byte_perm(t2, t3, 0x5410);
+        col[3][b] = __byte_perm(t2, t3, 0x7632);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        st_cs(reinterpret_cast<uint4*>(a.qt + (c_first + j) * a.M + r_first),
+              make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]));
+}
+
+template <int G>
+cudaError_t launch_act(const ActArgs& a, cudaStream_t s) {
+    const dim3 grid((unsigned)((a.N + kTileC - 1) / kTileC), (unsigned)((a.M + kTileR - 1) / kTileR));
+    act_quant_kernel<G><<<grid, kActThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_act_quant(const ActArgs& a, int G, cudaStream_t s) {
+    switch (G) {
+        case 4: return launch_act<4>(a, s);
+        case 8: return launch_act<8>(a, s);
+        case 16: return launch_act<16>(a, s);
+        case 32: return launch_act<32>(a, s);
+        case 64: return launch_act<64>(a, s);
+        case 128: return launch_act<128>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace coat

@@ -138,6 +138,25 @@ coat_status coat_fp8_quantize_absmax(const float* x, int64_t n, int32_t G, uint8
     return from_cuda(coat::launch_absmax_quantize(a, G, static_cast<cudaStream_t>(stream)));
 }
 
+coat_status coat_act_quantize_fp8(const uint16_t* x, int64_t M, int64_t N, int32_t G, uint8_t* q,
+                                  uint8_t* qt, float* scale, void* stream) {
+    if (!x || !q || !scale || M < 1 || N < 1) return COAT_ERR_INVALID_ARG;
+    if (G < 4 || G > 128 || (G & (G - 1)) != 0) return COAT_ERR_UNSUPPORTED_G;
+    if (M % 16 != 0 || N % 16 != 0 || N % G != 0) return COAT_ERR_INVALID_ARG;
+    if (M > 65535LL * 64 || N / 128 >= (1LL << 31)) return COAT_ERR_INVALID_ARG;   // grid limits
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scale) || (qt && !aligned16(qt)))
+        return COAT_ERR_MISALIGNED;
+    const size_t ne = (size_t)M * (size_t)N, ns = ne / (size_t)G;
+    if (overlaps(x, 2 * ne, q, ne) || overlaps(x, 2 * ne, scale, 4 * ns) ||
+        overlaps(q, ne, scale, 4 * ns) ||
+        (qt && (overlaps(qt, ne, x, 2 * ne) || overlaps(qt, ne, q, ne) || overlaps(qt, ne, scale, 4 * ns))))
+        return COAT_ERR_INVALID_ARG;
+    if (!is_device(x) || !is_device(q) || !is_device(scale) || (qt && !is_device(qt)))
+        return COAT_ERR_NOT_DEVICE;
+    coat::ActArgs a{x, M, N, q, qt, scale};
+    return from_cuda(coat::launch_act_quant(a, G, static_cast<cudaStream_t>(stream)));
+}
+
 coat_status coat_dre_dequantize(const uint8_t* q, const float* scale, const float* k, int64_t n,
                                 int32_t G, float* x, void* stream) {
     if (!x || !q || !scale || !k || n < 1) return COAT_ERR_INVALID_ARG;

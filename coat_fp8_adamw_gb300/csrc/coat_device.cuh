@@ -270,6 +270,26 @@ __device__ __forceinline__ float expand_scaled_pos(float r, float k) {
     return ex2_approx(fmaf(k, lg2_approx(r), kLog2_448));
 }
 
+// x / S ready for an E4M3 round-to-nearest-even conversion that rounds the
+// EXACT quotient.  y = RN(x / S) can land exactly on a midpoint between two
+// E4M3 values when the exact quotient lies just beside it; the exact remainder
+// x - y S (an FMA, exact for a rounded quotient) tells which side, and y moves
+// one float step that way.  No other midpoint can lie between y and the exact
+// quotient (midpoints are floats, and the quotient is within half a float step
+// of y), so this only matters when y is a midpoint.  Midpoints: 4 significant
+// bits with the 4th set for |y| >= 2^-6, odd multiples of 2^-10 below.  S > 0.
+__device__ __forceinline__ float e4m3_quotient(float x, float S) {
+    const float y = __fdiv_rn(x, S);
+    const float ay = fabsf(y);
+    const uint32_t b = __float_as_uint(ay);
+    const float t = ay * 1024.0f;
+    const bool mid = ay >= 0.015625f ? (b & 0xFFFFFu) == 0x80000u
+                                     : (t == rintf(t) && (((uint32_t)t) & 1u) != 0u);
+    const float r = fmaf(-y, S, x);
+    if (!mid || r == 0.0f) return y;
+    return __uint_as_float(__float_as_uint(y) + (((r > 0.0f) == (y > 0.0f)) ? 1u : 0xFFFFFFFFu));
+}
+
 // Smallest-non-zero tracking: fp32 magnitudes as unsigned bits minus one, so
 // that zero wraps to 0xFFFFFFFF and never wins a min.
 __device__ __forceinline__ uint32_t nz_key(float a) { return __float_as_uint(a) - 1u; }

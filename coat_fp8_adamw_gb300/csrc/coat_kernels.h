@@ -54,7 +54,16 @@ coat_status check_step_args(const float* w, const uint16_t* g, const uint8_t* m_
 // per-launch constants of the step (everything but the buffers)
 coat_status make_step_args(float beta1, float beta2, float lr, float eps, float weight_decay,
                            int64_t step, StepArgs& a);
+struct ActArgs {
+    const uint16_t* x;   // M x N bf16, row-major
+    int64_t M, N;
+    uint8_t* q;          // M x N codes
+    uint8_t* qt;         // N x M codes (may be null)
+    float* scale;        // M x N/G
+};
+
 cudaError_t launch_dre_quantize(const QuantArgs& a, int G, cudaStream_t stream);
+cudaError_t launch_act_quant(const ActArgs& a, int G, cudaStream_t stream);
 cudaError_t launch_absmax_quantize(const QuantArgs& a, int G, cudaStream_t stream);
 cudaError_t launch_dre_dequantize(const DequantArgs& a, int G, cudaStream_t stream);
 

@@ -189,8 +189,8 @@ absmax_quantize_kernel(const QuantArgs a) {
     for (int e = 0; e < kVec; e += 2) {
         const int j0 = e / Gm::kElems, j1 = (e + 1) / Gm::kElems;
         // +0 for a zero (or an all-zero group): the code of a zero is 0x00
-        const float y0 = S[j0] > 0.0f ? __fadd_rn(__fdiv_rn(x[e], S[j0]), 0.0f) : 0.0f;
-        const float y1 = S[j1] > 0.0f ? __fadd_rn(__fdiv_rn(x[e + 1], S[j1]), 0.0f) : 0.0f;
+        const float y0 = S[j0] > 0.0f ? __fadd_rn(e4m3_quotient(x[e], S[j0]), 0.0f) : 0.0f;
+        const float y1 = S[j1] > 0.0f ? __fadd_rn(e4m3_quotient(x[e + 1], S[j1]), 0.0f) : 0.0f;
         const uint32_t p = e4m3x2(y0, y1);
         if ((e & 2) == 0) out[e / 4] = p; else out[e / 4] |= p << 16;
     }

@@ -200,6 +200,27 @@ coat_status coat_fp8_quantize_absmax(const float *x, int64_t n, int32_t G, uint8
                                      float *scale, void *stream);
 
 /*
+ * Per-group (1 x G) FP8 quantization of an activation with a transposed FP8
+ * second output (COAT review page, section 4, "non-linear layer optimisation":
+ * a quantized FP8 output plus a transposed FP8 output for the backward pass,
+ * groups along the last dimension, two-stage maximum; the section 5 group-size
+ * table sweeps G = 4 ... 64 and 1 x 128).  Each row of x is split into groups
+ * of G consecutive elements: scale = max|x| / 448 rounded to float, and
+ * q = E4M3(x / scale) rounded to nearest even, saturating; an all-zero group
+ * has scale 0 and zero codes.
+ *   x      [M x N] bfloat16 (raw 16-bit patterns), row-major, in.
+ *   q      [M x N] uint8 out: the codes in the layout of x.
+ *   qt     [N x M] uint8 out: the same codes transposed (qt[c*M + r] = q[r*N + c]);
+ *          NULL to skip it.
+ *   scale  [M x N/G] float32 out, row-major (group g of row r at r*N/G + g).
+ *   G a power of two in [4, 128]; M and N multiples of 16; N a multiple of G;
+ *   M <= 4,194,240 (65535 tiles of 64 rows).
+ * The outputs must not overlap x or each other.
+ */
+coat_status coat_act_quantize_fp8(const uint16_t *x, int64_t M, int64_t N, int32_t G, uint8_t *q,
+                                  uint8_t *qt, float *scale, void *stream);
+
+/*
  * Inverse of coat_dre_quantize: x = sign(q) (|E4M3(q)| scale)^(1/k).
  *   q [n] uint8 in;  scale, k [ceil(n/G)] float32 in (k > 0);  x [n] float32 out.
  */

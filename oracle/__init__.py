@@ -186,6 +186,19 @@ def absmax_quantize(x: np.ndarray, G: int, nthreads: int = 0):
     return q, S
 
 
+def act_quantize(x_bf16_bits: np.ndarray, G: int, nthreads: int = 0):
+    """Per-group (1 x G) FP8 quantization of an M x N bf16 activation (raw bits)
+    -> (q [M, N], qt [N, M], S [M, N/G]): each row split into groups of G
+    columns, quantized like :func:`absmax_quantize`; qt is q transposed."""
+    M, N = x_bf16_bits.shape
+    if N % G:
+        raise ValueError("oracle act_quantize: N must be a multiple of G")
+    x = (x_bf16_bits.astype(np.uint32) << 16).view(np.float32).ravel()
+    q, S = absmax_quantize(x, G, nthreads)
+    q = q.reshape(M, N)
+    return q, np.ascontiguousarray(q.T), S.reshape(M, N // G)
+
+
 def dre_dequantize(q: np.ndarray, S: np.ndarray, k: np.ndarray, G: int,
                    nthreads: int = 0) -> np.ndarray:
     """Inverse of :func:`dre_quantize`: sign(q) (|dec(q)| S)^(1/k) rounded to fp32."""

@@ -82,3 +82,21 @@ def test_special_groups():
 def test_bad_arguments():
     with pytest.raises(ValueError):
         oracle.absmax_quantize(np.zeros(0, np.float32), 16)
+
+
+def test_activation_groups_run_along_rows():
+    """The activation quantizer groups G consecutive columns of one row; its
+    second output is the first one transposed."""
+    rng = np.random.default_rng(4)
+    M, N, G = 32, 64, 16
+    row_scale = 2.0 ** rng.integers(-20, 5, size=(M, N // G))     # one magnitude per row group
+    x = np.repeat(row_scale, G, axis=1) * rng.uniform(-1, 1, size=(M, N))
+    x[:, ::G] = np.repeat(row_scale, 1, axis=1) * 448 / 256       # a known max in each group
+    bits = (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)   # truncate to bf16
+    xb = (bits.astype(np.uint32) << 16).view(np.float32)
+    q, qt, S = oracle.act_quantize(bits, G)
+    expect_S = (np.abs(xb).reshape(M, N // G, G).max(axis=2).astype(np.float64) / 448).astype(np.float32)
+    assert np.array_equal(S, expect_S)
+    assert np.array_equal(qt, q.T)
+    # each group's largest element sits at the top of the grid
+    assert np.all(np.abs(q.reshape(M, N // G, G).astype(int) & 0x7F).max(axis=2) == 0x7E)
