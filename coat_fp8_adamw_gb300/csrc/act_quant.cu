@@ -61,7 +61,7 @@ act_quant_kernel(const ActArgs a) {
         }
         constexpr int kGroupsHere = G >= 8 ? 1 : 8 / G;   // groups in this thread's 8 elements
         constexpr int kPer = G >= 8 ? 8 : G;               // elements of one group here
-        float S[kGroupsHere];
+        float S[kGroupsHere], inv[kGroupsHere];
 #pragma unroll
         for (int j = 0; j < kGroupsHere; ++j) {
             float mx = 0.0f;
@@ -73,16 +73,27 @@ act_quant_kernel(const ActArgs a) {
                     mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
             }
             S[j] = __fdiv_rn(mx, 448.0f);
+            inv[j] = rcp_approx(S[j]);
         }
-        uint32_t codes[2];
+        uint32_t codes[2] = {0u, 0u}, und = 0u;
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            const float s0 = S[e / kPer], s1 = S[(e + 1) / kPer];
-            // +0 for a zero (or an all-zero group): the code of a zero is 0x00
-            const float y0 = s0 > 0.0f ? __fadd_rn(e4m3_quotient(x[e], s0), 0.0f) : 0.0f;
-            const float y1 = s1 > 0.0f ? __fadd_rn(e4m3_quotient(x[e + 1], s1), 0.0f) : 0.0f;
-            const uint32_t pr = e4m3x2(y0, y1);
-            if ((e & 2) == 0) codes[e / 4] = pr; else codes[e / 4] |= pr << 16;
+        for (int e = 0; e < 8; ++e) {
+            bool u;
+            // an all-zero group keeps zero codes
+            const uint32_t c = e4m3_code_fast(x[e], inv[e / kPer], u);
+            if (S[e / kPer] > 0.0f) {
+                codes[e / 4] |= c << (8 * (e & 3));
+                und |= (u ? 1u : 0u) << e;
+            }
+        }
+        if (und) {   // rare: quotients beside a midpoint
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (und & (1u << e)) {
+                    const uint32_t c = e4m3_code_of_quotient_exact(x[e], S[e / kPer]);
+                    codes[e / 4] = (codes[e / 4] & ~(0xFFu << (8 * (e & 3)))) | (c << (8 * (e & 3)));
+                }
+            }
         }
         const int tr = 8 * p + r_in;
         tile[tr * kPitchW + c8 / 4] = codes[0];

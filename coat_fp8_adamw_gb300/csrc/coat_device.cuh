@@ -290,6 +290,25 @@ __device__ __forceinline__ float e4m3_quotient(float x, float S) {
     return __uint_as_float(__float_as_uint(y) + (((r > 0.0f) == (y > 0.0f)) ? 1u : 0xFFFFFFFFu));
 }
 
+// E4M3 codes (round to nearest even, saturating, 0x00 for a zero) of the
+// exact quotients x / S, S > 0, given inv ~ 1/S from the SFU (at most one
+// float step off).  y = RN(x inv) is within 2.5 float steps of x / S;
+// y (1 - 2^-20) and y (1 + 2^-20) lie at least 7.5 steps below and above it,
+// so when both convert to the same code no E4M3 midpoint separates y from
+// the exact quotient and that code is the answer.  The other elements (a
+// midpoint within a few steps, or an SFU reciprocal that is not finite) are
+// flagged in `undecided` and left to e4m3_code_of_quotient_exact.
+__device__ __forceinline__ uint32_t e4m3_code_fast(float x, float inv, bool& undecided) {
+    const float y = fmaf(x, inv, 0.0f);   // +0 for a zero of either sign
+    const uint32_t p = e4m3x2(y * 0.99999904632568359f, y * 1.00000095367431641f);
+    undecided = (p & 0xFFu) != (p >> 8) || !(inv <= 3.40282347e38f);
+    return p & 0xFFu;
+}
+// The rare case, out of line so that it stays a branch taken by few lanes.
+static __device__ __noinline__ uint32_t e4m3_code_of_quotient_exact(float x, float S) {
+    return e4m3x2(__fadd_rn(e4m3_quotient(x, S), 0.0f), 0.0f) & 0xFFu;
+}
+
 // Smallest-non-zero tracking: fp32 magnitudes as unsigned bits minus one, so
 // that zero wraps to 0xFFFFFFFF and never wins a min.
 __device__ __forceinline__ uint32_t nz_key(float a) { return __float_as_uint(a) - 1u; }

@@ -179,20 +179,34 @@ absmax_quantize_kernel(const QuantArgs a) {
 #pragma unroll
     for (int off = Gm::kLanes / 2; off > 0; off >>= 1)
         mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xFFFFFFFFu, mx[0], off));
-    float S[Gm::kGroups];
+    float S[Gm::kGroups], inv[Gm::kGroups];
 #pragma unroll
-    for (int j = 0; j < Gm::kGroups; ++j) S[j] = __fdiv_rn(mx[j], 448.0f);
+    for (int j = 0; j < Gm::kGroups; ++j) {
+        S[j] = __fdiv_rn(mx[j], 448.0f);
+        inv[j] = rcp_approx(S[j]);
+    }
     if (!active) return;
 
-    uint32_t out[kVec / 4];
+    uint32_t out[kVec / 4] = {0u, 0u, 0u, 0u}, und = 0u;
 #pragma unroll
-    for (int e = 0; e < kVec; e += 2) {
-        const int j0 = e / Gm::kElems, j1 = (e + 1) / Gm::kElems;
-        // +0 for a zero (or an all-zero group): the code of a zero is 0x00
-        const float y0 = S[j0] > 0.0f ? __fadd_rn(e4m3_quotient(x[e], S[j0]), 0.0f) : 0.0f;
-        const float y1 = S[j1] > 0.0f ? __fadd_rn(e4m3_quotient(x[e + 1], S[j1]), 0.0f) : 0.0f;
-        const uint32_t p = e4m3x2(y0, y1);
-        if ((e & 2) == 0) out[e / 4] = p; else out[e / 4] |= p << 16;
+    for (int e = 0; e < kVec; ++e) {
+        const int j = e / Gm::kElems;
+        bool u;
+        // an all-zero group keeps zero codes
+        const uint32_t c = e4m3_code_fast(x[e], inv[j], u);
+        if (S[j] > 0.0f) {
+            out[e / 4] |= c << (8 * (e & 3));
+            und |= (u ? 1u : 0u) << e;
+        }
+    }
+    if (und) {   // rare: quotients beside a midpoint
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            if (und & (1u << e)) {
+                const uint32_t c = e4m3_code_of_quotient_exact(x[e], S[e / Gm::kElems]);
+                out[e / 4] = (out[e / 4] & ~(0xFFu << (8 * (e & 3)))) | (c << (8 * (e & 3)));
+            }
+        }
     }
     if (full) {
         st_cs(reinterpret_cast<uint4*>(a.q + base), make_uint4(out[0], out[1], out[2], out[3]));
