@@ -48,6 +48,24 @@
 
 namespace coat {
 
+// The tables of the exact path, in global memory: only the few lanes that
+// re-evaluate candidates (and the per-group jobs) read them, through L1, so
+// the step kernel's shared memory can hold the inputs of that path instead.
+namespace gtab {
+#undef COAT_CONST
+#define COAT_CONST __device__
+#include "coat_tables.inc"
+#undef COAT_CONST
+#define COAT_CONST __constant__
+}  // namespace gtab
+
+__device__ __forceinline__ df::Tables global_tables() {
+    return df::Tables{reinterpret_cast<const float*>(gtab::kLog2CenterHi),
+                      reinterpret_cast<const float*>(gtab::kLog2CenterLo),
+                      reinterpret_cast<const float*>(gtab::kExp2FracHi),
+                      reinterpret_cast<const float*>(gtab::kExp2FracLo)};
+}
+
 namespace {
 
 using df::F2;
@@ -403,10 +421,10 @@ struct CtaLayout {
     static constexpr int L = G / kVec;          // lanes per group
     static constexpr size_t off_m = 0;
     static constexpr size_t off_v = off_m + (size_t)CTA * kVec * 4;
-    static constexpr size_t off_grp = off_v + (size_t)CTA * kVec * 4;
+    static constexpr size_t off_in = off_v + (size_t)CTA * kVec * 4;   // g, m codes, v codes per thread
+    static constexpr size_t off_grp = off_in + (size_t)CTA * 64;
     static constexpr size_t off_lg = off_grp + (size_t)NGC * sizeof(GroupRec);
-    static constexpr size_t off_tab = off_lg + 2 * 128 * 4;
-    static constexpr size_t bytes = off_tab + sizeof(SmemTables);
+    static constexpr size_t bytes = off_lg + 128 * 4;
 };
 
 template <int G, int CTA>
@@ -418,15 +436,15 @@ step_kernel_cta(const StepArgs a) {
     constexpr int NGC = Lay::NGC;
     constexpr int L = Lay::L;
     static_assert(L >= 1 && L <= 16 && (Lay::off_v % 16) == 0 && (Lay::off_grp % 16) == 0 &&
-                      (Lay::off_lg % 4) == 0,
+                      (Lay::off_in % 16) == 0 && (Lay::off_lg % 4) == 0,
                   "shared-memory layout");
     extern __shared__ __align__(16) unsigned char smem[];
     float(*sm_m)[kVec] = reinterpret_cast<float(*)[kVec]>(smem + Lay::off_m);
     float(*sm_v)[kVec] = reinterpret_cast<float(*)[kVec]>(smem + Lay::off_v);
     GroupRec* grp = reinterpret_cast<GroupRec*>(smem + Lay::off_grp);
+    uint4* sm_in = reinterpret_cast<uint4*>(smem + Lay::off_in);   // 4 x 16 bytes per thread
     float* lg_hi = reinterpret_cast<float*>(smem + Lay::off_lg);
-    float* lg_lo = lg_hi + 128;
-    SmemTables& st = *reinterpret_cast<SmemTables*>(smem + Lay::off_tab);
+    const float* lg_lo = reinterpret_cast<const float*>(gtab::kLog2Frac448Lo);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t cta_base = (int64_t)blockIdx.x * kCtaElems;
@@ -440,13 +458,9 @@ step_kernel_cta(const StepArgs a) {
     if (active) load_chunk(a, base, full, c);
     else zero_chunk(c);
 
-    for (int i = tid; i < 128; i += kCta) {
-        lg_hi[i] = __uint_as_float(kLog2Frac448Hi[i]);
-        lg_lo[i] = __uint_as_float(kLog2Frac448Lo[i]);
-    }
-    load_smem_tables(st, tid, kCta);
+    for (int i = tid; i < 128; i += kCta) lg_hi[i] = __uint_as_float(kLog2Frac448Hi[i]);
     __syncthreads();
-    const df::Tables tab = tables_of(st);
+    const df::Tables tab = global_tables();
 
     // ---- B: stored-state parameters, one job per (group, moment) ----
     for (int j = tid; j < 2 * NGC; j += kCta) {
@@ -499,6 +513,11 @@ step_kernel_cta(const StepArgs a) {
             *reinterpret_cast<float4*>(&sm_v[tid][slot]) = make_float4(vt[0], vt[1], vt[2], vt[3]);
         }
         if (active) store_w(a, base, full, c);
+        // the inputs of the exact pass: this thread's gradients and codes
+        sm_in[4 * tid + 0] = make_uint4(c.g[0], c.g[1], c.g[2], c.g[3]);
+        sm_in[4 * tid + 1] = make_uint4(c.g[4], c.g[5], c.g[6], c.g[7]);
+        sm_in[4 * tid + 2] = make_uint4(c.mq[0], c.mq[1], c.mq[2], c.mq[3]);
+        sm_in[4 * tid + 3] = make_uint4(c.vq[0], c.vq[1], c.vq[2], c.vq[3]);
 
         // stage 2 across the lanes of the group
         float fmx_m = lmx_m, fmx_v = lmx_v, gmx = lmx_g, fmn_m = lmn_m, fmn_v = lmn_v;
@@ -564,25 +583,15 @@ step_kernel_cta(const StepArgs a) {
             const int ln = __ffs(h) - 1;
             h &= h - 1u;
             const int th = (int)r.hwarp * 32 + ln;
-            const int64_t tb = cta_base + (int64_t)th * kVec;
             float* vals = second ? sm_v[th] : sm_m[th];
-            // the holder's gradients and codes, read again (this CTA just streamed them)
+            // the holder's gradients and codes, from shared memory (zero beyond n)
             uint32_t gw[8], cw[4];
-            if (tb + kVec <= a.n) {
-                const uint4 g0 = __ldg(reinterpret_cast<const uint4*>(a.g + tb));
-                const uint4 g1 = __ldg(reinterpret_cast<const uint4*>(a.g + tb) + 1);
-                // the codes are rewritten by this kernel (phase F): no read-only path
-                const uint4 cc = __ldcg(reinterpret_cast<const uint4*>((second ? a.vq : a.mq) + tb));
+            {
+                const uint4 g0 = sm_in[4 * th], g1 = sm_in[4 * th + 1];
+                const uint4 cc = sm_in[4 * th + (second ? 3 : 2)];
                 gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
                 gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
                 cw[0] = cc.x; cw[1] = cc.y; cw[2] = cc.z; cw[3] = cc.w;
-            } else {
-                for (int i = 0; i < 8; ++i) gw[i] = 0u;
-                for (int i = 0; i < 4; ++i) cw[i] = 0u;
-                for (int e = 0; e < kVec && tb + e < a.n; ++e) {
-                    gw[e / 2] |= (uint32_t)a.g[tb + e] << (16 * (e & 1));
-                    cw[e / 4] |= (uint32_t)(second ? a.vq : a.mq)[tb + e] << (8 * (e & 3));
-                }
             }
             uint32_t msk = 0u;
 #pragma unroll

@@ -70,12 +70,15 @@ def _llama_like(name: str, layers: int, d: int, mlp: int, vocab: int, tied: bool
 
 
 def workload(name: str, G: Optional[int] = None) -> Workload:
-    """The five parameter sets.
+    """The parameter sets.
 
     * ``tiny``     one tensor of 4096 params; g ~ N(0, 1e-3^2) with 1% x100
                    outliers; group 30 all-zero gradient, group 31 one non-zero.
     * ``mat4096``  one 4096x4096 matrix; row r has g ~ N(0, s_r^2),
                    s_r log-uniform in [1e-5, 1e-2].
+    * ``mat16384`` one 16384x16384 matrix (3.8 GB of state: every access goes to
+                   HBM, yet small enough for a full profiler capture); gradients
+                   like the model-shaped sets (log-normal scale, 0.1% x1000).
     * ``olmo1b``   OLMo-1B-shaped: 16 layers, d=2048, MLP 8192, tied vocab 50304.
     * ``llama7b``  Llama-2-7B-shaped: 32 layers, d=4096, MLP 11008, vocab 32000.
     * ``llama13b`` Llama-2-13B-shaped: 40 layers, d=5120, MLP 13824, vocab 32000.
@@ -84,6 +87,8 @@ def workload(name: str, G: Optional[int] = None) -> Workload:
         return Workload("tiny", (Tensor("w", 4096),), G or 128, 0, "tiny")
     if name == "mat4096":
         return Workload("mat4096", (Tensor("w", 4096 * 4096),), G or 128, 1, "rowscale")
+    if name == "mat16384":
+        return Workload("mat16384", (Tensor("w", 16384 * 16384),), G or 128, 5, "lognormal")
     if name == "olmo1b":
         return _llama_like("olmo1b", 16, 2048, 8192, 50304, True, G or 128, 2)
     if name == "llama7b":
@@ -93,7 +98,7 @@ def workload(name: str, G: Optional[int] = None) -> Workload:
     raise KeyError(name)
 
 
-WORKLOADS = ("tiny", "mat4096", "olmo1b", "llama7b", "llama13b")
+WORKLOADS = ("tiny", "mat4096", "mat16384", "olmo1b", "llama7b", "llama13b")
 
 
 # ---------------------------------------------------------------------------
