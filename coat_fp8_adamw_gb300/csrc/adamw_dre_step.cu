@@ -29,17 +29,18 @@
 // S are formed from them in double-float and rounded once, and the
 // re-evaluated elements are encoded from their exact values.
 //
-// Execution.  A CTA of 256 threads owns 4096 consecutive parameters (16 per
-// thread: every stream is whole 128-bit accesses).  The per-group work runs
-// as CTA-wide jobs between barriers -- one thread per (group, moment) or per
-// (group, statistic) -- so that it occupies a few full warps instead of a few
-// lanes of every warp; the moments wait in shared memory between phases.
-//   B  stored-state parameters            2 jobs per group
-//   C  fast path, statistics, candidates   every thread
-//   D1 candidate masks                     4 jobs per group
-//   D2 exact re-evaluation                 4 jobs per group
-//   E  k, S, encoding constants, record    2 jobs per group
-//   F  encode and store codes              every thread
+// Execution.  A CTA of 128 threads owns 2048 consecutive parameters (16 per
+// thread: every stream is whole 128-bit accesses); eight CTAs share an SM.
+// The per-group work runs as CTA-wide jobs between barriers -- one thread per
+// (group, moment) or per (group, statistic) -- so that it occupies a few full
+// warps instead of a few lanes of every warp.  The moments wait in shared
+// memory between phases, next to a copy of each thread's gradients and codes
+// for the exact pass.
+//   B  stored-state parameters                      2 jobs per group
+//   C  fast path, statistics, candidate holders      every thread
+//   D  candidate masks and exact re-evaluation       4 jobs per group
+//   E  k, S, encoding constants, record              2 jobs per group
+//   F  encode and store codes                        every thread
 // Groups of G < 16 parameters live inside one thread (step_kernel_thread).
 #include <cstddef>
 
@@ -74,7 +75,7 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 #ifndef COAT_STEP_CTA
 #define COAT_STEP_CTA 128
 #endif
-constexpr int kStepCta = COAT_STEP_CTA;    // threads per CTA of the cooperative kernel
+constexpr int kStepCta = COAT_STEP_CTA;    // threads per CTA of the step kernel
 #define kInf __int_as_float(0x7F800000)
 
 // Relative error bound of the SFU exp2 (ex2.approx.ftz.f32), with margin.
