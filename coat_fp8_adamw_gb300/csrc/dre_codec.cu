@@ -16,6 +16,9 @@ struct Geom {
     static constexpr int kLanes = G >= kVec ? G / kVec : 1;
     static constexpr int kGroups = G >= kVec ? 1 : kVec / G;
     static constexpr int kElems = G >= kVec ? kVec : G;
+    // several lanes share a group: its parameters are formed once per CTA job
+    static constexpr bool kJobs = G >= 2 * kVec;
+    static constexpr int kGpc = kJobs ? kThreads * kVec / G : 1;   // groups per CTA
 };
 
 template <int G>
@@ -23,12 +26,15 @@ __global__ void __launch_bounds__(kThreads)
 dre_quantize_kernel(const QuantArgs a) {
     using Gm = Geom<G>;
     __shared__ SmemTables st;
+    __shared__ float s_mx[Gm::kGpc], s_k[Gm::kGpc], s_inv[Gm::kGpc], s_pre[Gm::kGpc];
+    __shared__ uint32_t s_mn[Gm::kGpc];
     load_smem_tables(st, threadIdx.x, kThreads);
     __syncthreads();
     const df::Tables tab = tables_of(st);
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t base = tid * kVec;
-    if (__all_sync(0xFFFFFFFFu, base >= a.n)) return;
+    // the job phase below has CTA barriers: only the per-lane form may leave early
+    if (!Gm::kJobs && __all_sync(0xFFFFFFFFu, base >= a.n)) return;
     const bool active = base < a.n;
     const bool full = base + kVec <= a.n;
 
@@ -63,13 +69,45 @@ dre_quantize_kernel(const QuantArgs a) {
     }
     QuantParams qp[Gm::kGroups];
     float pre[Gm::kGroups];
+    if constexpr (Gm::kJobs) {
+        // one thread per group of the CTA forms k, S and the encoding
+        // constants (the lanes of a group would otherwise each repeat them)
+        const int gl = (int)((threadIdx.x * kVec) / G);
+        if ((threadIdx.x * kVec) % G == 0) {
+            s_mx[gl] = mx[0];
+            s_mn[gl] = mn[0];
+        }
+        __syncthreads();
+        const int64_t gcta = (int64_t)blockIdx.x * Gm::kGpc;
+        for (int j = threadIdx.x; j < Gm::kGpc; j += kThreads) {
+            const float gm = s_mx[j];
+            QuantParams q = quant_params_precise(gm, nz_key_value(s_mn[j]), tab);
+            float pr = 1.0f;
+            if (gm > 0.0f && gm < 1.17549435e-38f) {
+                pr = 16777216.0f;
+                q.inv_mx = __frcp_rn(gm * 16777216.0f);
+            }
+            s_k[j] = q.k;
+            s_inv[j] = q.inv_mx;
+            s_pre[j] = pr;
+            if ((gcta + j) * G < a.n) {
+                a.scale[gcta + j] = q.S;
+                a.k[gcta + j] = q.k;
+            }
+        }
+        __syncthreads();
+        qp[0].k = s_k[gl];
+        qp[0].inv_mx = s_inv[gl];
+        pre[0] = s_pre[gl];
+    } else {
 #pragma unroll
-    for (int j = 0; j < Gm::kGroups; ++j) {
-        qp[j] = quant_params_precise(mx[j], nz_key_value(mn[j]), tab);
-        pre[j] = 1.0f;
-        if (mx[j] > 0.0f && mx[j] < 1.17549435e-38f) {
-            pre[j] = 16777216.0f;
-            qp[j].inv_mx = __frcp_rn(mx[j] * 16777216.0f);
+        for (int j = 0; j < Gm::kGroups; ++j) {
+            qp[j] = quant_params_precise(mx[j], nz_key_value(mn[j]), tab);
+            pre[j] = 1.0f;
+            if (mx[j] > 0.0f && mx[j] < 1.17549435e-38f) {
+                pre[j] = 16777216.0f;
+                qp[j].inv_mx = __frcp_rn(mx[j] * 16777216.0f);
+            }
         }
     }
     if (!active) return;
@@ -90,12 +128,14 @@ dre_quantize_kernel(const QuantArgs a) {
         for (int e = 0; e < kVec; ++e)
             if (base + e < a.n) a.q[base + e] = (uint8_t)(out[e / 4] >> (8 * (e & 3)));
     }
-    const int64_t g0 = base / G;
-    const bool leader = G >= kVec ? ((base % G) == 0) : true;
-    if (leader) {
+    if constexpr (!Gm::kJobs) {
+        const int64_t g0 = base / G;
+        const bool leader = G >= kVec ? ((base % G) == 0) : true;
+        if (leader) {
 #pragma unroll
-        for (int j = 0; j < Gm::kGroups; ++j)
-            if ((g0 + j) * G < a.n) { a.scale[g0 + j] = qp[j].S; a.k[g0 + j] = qp[j].k; }
+            for (int j = 0; j < Gm::kGroups; ++j)
+                if ((g0 + j) * G < a.n) { a.scale[g0 + j] = qp[j].S; a.k[g0 + j] = qp[j].k; }
+        }
     }
 }
 
@@ -104,7 +144,19 @@ __global__ void __launch_bounds__(kThreads)
 dre_dequantize_kernel(const DequantArgs a) {
     using Gm = Geom<G>;
     __shared__ float s_log[128];
+    __shared__ float s_P[Gm::kGpc], s_rk[Gm::kGpc];
     for (int i = threadIdx.x; i < 128; i += kThreads) s_log[i] = __uint_as_float(kLog2Frac448Hi[i]);
+    if constexpr (Gm::kJobs) {
+        // one thread per group of the CTA forms its dequantization parameters
+        const int64_t gcta = (int64_t)blockIdx.x * Gm::kGpc;
+        for (int j = threadIdx.x; j < Gm::kGpc; j += kThreads) {
+            float S = 0.0f, k = 1.0f;
+            if ((gcta + j) * G < a.n) { S = a.scale[gcta + j]; k = a.k[gcta + j]; }
+            const DequantParams d = dequant_params(S, k);
+            s_P[j] = d.P;
+            s_rk[j] = d.rk;
+        }
+    }
     __syncthreads();
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t base = tid * kVec;
@@ -123,11 +175,17 @@ dre_dequantize_kernel(const DequantArgs a) {
     }
     const int64_t g0 = base / G;
     DequantParams d[Gm::kGroups];
+    if constexpr (Gm::kJobs) {
+        const int gl = (int)((threadIdx.x * kVec) / G);
+        d[0].P = s_P[gl];
+        d[0].rk = s_rk[gl];
+    } else {
 #pragma unroll
-    for (int j = 0; j < Gm::kGroups; ++j) {
-        float S = 0.0f, k = 1.0f;
-        if ((g0 + j) * G < a.n) { S = a.scale[g0 + j]; k = a.k[g0 + j]; }
-        d[j] = dequant_params(S, k);
+        for (int j = 0; j < Gm::kGroups; ++j) {
+            float S = 0.0f, k = 1.0f;
+            if ((g0 + j) * G < a.n) { S = a.scale[g0 + j]; k = a.k[g0 + j]; }
+            d[j] = dequant_params(S, k);
+        }
     }
     float x[kVec];
 #pragma unroll
