@@ -24,6 +24,46 @@ namespace coat {
 
 namespace {
 
+// Packed fp32 pairs (PTX .f32x2): each half rounds like the scalar instruction.
+__device__ __forceinline__ uint64_t pk(float x, float y) {
+    uint64_t u;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(x), "f"(y));
+    return u;
+}
+__device__ __forceinline__ void upk(uint64_t u, float& x, float& y) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(u));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// RN(m / 448) for a bf16 group maximum m >= 0: q = RN(m y) with y = RN(1/448),
+// then one FMA correction from the exact remainder m - q 448 (Markstein's
+// division by a known divisor).  Checked against the correctly rounded
+// quotient for every non-negative finite bf16 value, subnormals included.
+constexpr float kInv448 = 1.0f / 448.0f;
+__device__ __forceinline__ float div448_bf16(float m) {
+    const float q = __fmul_rn(m, kInv448);
+    const float r = fmaf(-q, 448.0f, m);
+    return fmaf(r, kInv448, q);
+}
+
+// y (1 - 2^-20) and y (1 + 2^-20): see e4m3_code_fast
+constexpr float kDn = 0.99999904632568359f;
+constexpr float kUp = 1.00000095367431641f;
+
 constexpr int kTileR = 64;                  // rows per tile
 constexpr int kTileC = 128;                 // columns per tile
 constexpr int kActThreads = 128;
@@ -62,36 +102,43 @@ act_quant_kernel(const ActArgs a) {
         constexpr int kGroupsHere = G >= 8 ? 1 : 8 / G;   // groups in this thread's 8 elements
         constexpr int kPer = G >= 8 ? 8 : G;               // elements of one group here
         float S[kGroupsHere], inv[kGroupsHere];
+        bool inv_bad = false;
 #pragma unroll
         for (int j = 0; j < kGroupsHere; ++j) {
             float mx = 0.0f;
 #pragma unroll
-            for (int e = 0; e < kPer; ++e) mx = fmaxf(mx, fabsf(x[j * kPer + e]));
+            for (int e = 0; e < kPer; e += 2) mx = max3(mx, fabsf(x[j * kPer + e]), fabsf(x[j * kPer + e + 1]));
             if constexpr (G > 8) {
 #pragma unroll
                 for (int off = G / 16; off > 0; off >>= 1)
                     mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
             }
-            S[j] = __fdiv_rn(mx, 448.0f);
-            inv[j] = rcp_approx(S[j]);
+            S[j] = div448_bf16(mx);
+            // an all-zero group: inv = 0 keeps every code 0x00
+            inv[j] = S[j] > 0.0f ? rcp_approx(S[j]) : 0.0f;
+            inv_bad |= !(inv[j] <= 3.40282347e38f);
         }
-        uint32_t codes[2] = {0u, 0u}, und = 0u;
+        // codes of y (1 - 2^-20) and y (1 + 2^-20), two elements per conversion;
+        // a byte that differs marks an element whose code a midpoint decides
+        uint32_t codes[2] = {0u, 0u}, diff[2] = {0u, 0u};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            bool u;
-            // an all-zero group keeps zero codes
-            const uint32_t c = e4m3_code_fast(x[e], inv[e / kPer], u);
-            if (S[e / kPer] > 0.0f) {
-                codes[e / 4] |= c << (8 * (e & 3));
-                und |= (u ? 1u : 0u) << e;
-            }
+        for (int e = 0; e < 8; e += 2) {
+            const uint64_t yy = fma2(pk(x[e], x[e + 1]), pk(inv[e / kPer], inv[(e + 1) / kPer]),
+                                     pk(0.0f, 0.0f));   // +0 for a zero of either sign
+            float l0, l1, h0, h1;
+            upk(mul2(yy, pk(kDn, kDn)), l0, l1);
+            upk(mul2(yy, pk(kUp, kUp)), h0, h1);
+            const uint32_t clo = e4m3x2(l0, l1), chi = e4m3x2(h0, h1);
+            codes[e / 4] |= clo << (16 * ((e >> 1) & 1));
+            diff[e / 4] |= (clo ^ chi) << (16 * ((e >> 1) & 1));
         }
-        if (und) {   // rare: quotients beside a midpoint
+        if ((diff[0] | diff[1]) != 0u || inv_bad) {   // rare: quotients beside a midpoint
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                if (und & (1u << e)) {
-                    const uint32_t c = e4m3_code_of_quotient_exact(x[e], S[e / kPer]);
-                    codes[e / 4] = (codes[e / 4] & ~(0xFFu << (8 * (e & 3)))) | (c << (8 * (e & 3)));
+                const int sh = 8 * (e & 3);
+                if (((diff[e / 4] >> sh) & 0xFFu) != 0u || !(inv[e / kPer] <= 3.40282347e38f)) {
+                    const uint32_t c = S[e / kPer] > 0.0f ? e4m3_code_of_quotient_exact(x[e], S[e / kPer]) : 0u;
+                    codes[e / 4] = (codes[e / 4] & ~(0xFFu << sh)) | (c << sh);
                 }
             }
         }
