@@ -184,6 +184,9 @@ def recorded_traffic(workload: str, G: int):
 # ---------------------------------------------------------------------------
 # CPU baseline: the float64 oracle on a bounded sample of the workload
 # ---------------------------------------------------------------------------
+_CPU_SAMPLE = {}
+
+
 def cpu_baseline(workload: str, G: int, seconds: float):
     import numpy as np
 
@@ -191,10 +194,15 @@ def cpu_baseline(workload: str, G: int, seconds: float):
     from coat_fp8_adamw_gb300 import synth
     wl = synth.workload(workload, G)
     sample = min(wl.n, 1 << 24)          # a fixed contiguous slice of 2^24 parameters
-    rng = np.random.default_rng(0)
-    w = (rng.standard_normal(sample) * 0.02).astype(np.float32)
-    g = synth.f32_to_bf16_bits((rng.standard_normal(sample) * 1e-3).astype(np.float32))
-    mq, vq, meta = synth.random_state_np(sample, G, seed=1)
+    key = (sample, G)
+    if key not in _CPU_SAMPLE:           # generated once per process (reference-arm steps reuse it)
+        rng = np.random.default_rng(0)
+        w0 = (rng.standard_normal(sample) * 0.02).astype(np.float32)
+        g0 = synth.f32_to_bf16_bits((rng.standard_normal(sample) * 1e-3).astype(np.float32))
+        _CPU_SAMPLE.clear()
+        _CPU_SAMPLE[key] = (w0, g0) + tuple(synth.random_state_np(sample, G, seed=1))
+    w0, g, mq0, vq0, meta0 = _CPU_SAMPLE[key]
+    w, mq, vq, meta = w0.copy(), mq0.copy(), vq0.copy(), meta0.copy()
     hp = synth.HYPER
     threads = oracle.threads(0)
     done, t0, step = 0, time.perf_counter(), 1
