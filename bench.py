@@ -42,6 +42,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default="llama7b")
     p.add_argument("--G", type=int, default=128)
+    p.add_argument("--grads", type=int, default=3,
+                   help="distinct seeded gradients generated before timing and cycled through")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-e2e", action="store_true")
@@ -285,7 +287,11 @@ def run_ours(args):
     ng = coat.num_groups(n, G)
     hp = synth.HYPER
     w = synth.init_weights_torch(wl, dev)
-    g = synth.grad_torch(wl, 1, dev)
+    # a training run sees a new gradient every step: K distinct seeded
+    # gradients are generated before the timed region and cycled through
+    grads = [synth.grad_torch(wl, 1 + i, dev) for i in range(max(1, args.grads))]
+    n_grads = len(grads)
+    g = grads[0]
     mq = torch.zeros(n, dtype=torch.uint8, device=dev)
     vq = torch.zeros(n, dtype=torch.uint8, device=dev)
     meta = torch.zeros(ng, 4, dtype=torch.float32, device=dev)
@@ -296,8 +302,9 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     def step(t):
-        coat.coat_fp8_adamw_step(w, g, mq, vq, meta, G, hp["beta1"], hp["beta2"], hp["lr"],
-                                 hp["eps"], hp["weight_decay"], t, stream=stream)
+        coat.coat_fp8_adamw_step(w, grads[(t - 1) % len(grads)], mq, vq, meta, G, hp["beta1"],
+                                 hp["beta2"], hp["lr"], hp["eps"], hp["weight_decay"], t,
+                                 stream=stream)
 
     t = 0
     for _ in range(args.warmup):
@@ -341,6 +348,9 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     traffic_bpp = recorded_traffic(args.workload, G)
 
+    del grads[1:]            # the end-to-end leg streams the first gradient only
+    torch.cuda.empty_cache()
+
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
@@ -358,6 +368,7 @@ def run_ours(args):
                 "config": {"workload": f"{args.workload}-shaped parameter set", "G": G,
                            "params": n, "groups": ng, "bytes_per_param": bpp,
                            "parallelism": "replicas" if ws > 1 else "single GPU",
+                           "gradients": f"{n_grads} distinct seeded gradients, cycled",
                            "l2": l2_note(bpp * n)},
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
                              "unit": "GB/s", "frac": achieved / peak,
