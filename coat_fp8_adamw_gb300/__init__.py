@@ -124,10 +124,12 @@ def bytes_per_param(G: int) -> float:
 # torch-tensor front end
 # ---------------------------------------------------------------------------
 
-def _stream_ptr(stream) -> Optional[int]:
+def _stream_ptr(stream, device=None) -> Optional[int]:
+    """The stream handle to pass: ``stream``, or the current torch stream of
+    ``device`` (the device the tensors live on; the call runs with it current)."""
     import torch
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -164,9 +166,10 @@ def coat_fp8_adamw_step(w, g, m_q, v_q, meta, G: int, beta1: float, beta2: float
     pm = _check(m_q, torch.uint8, n, "m_q", dev)
     pv = _check(v_q, torch.uint8, n, "v_q", dev)
     pmeta = _check(meta, torch.float32, 4 * num_groups(n, G), "meta", dev)
-    st = lib().coat_fp8_adamw_step(pw, pg, pm, pv, pmeta, n, int(G), float(beta1), float(beta2),
-                                   float(lr), float(eps), float(weight_decay), int(step),
-                                   _stream_ptr(stream))
+    with torch.cuda.device(dev):
+        st = lib().coat_fp8_adamw_step(pw, pg, pm, pv, pmeta, n, int(G), float(beta1), float(beta2),
+                                       float(lr), float(eps), float(weight_decay), int(step),
+                                       _stream_ptr(stream))
     if st != 0:
         raise CoatError(st, "coat_fp8_adamw_step")
 
@@ -199,11 +202,12 @@ def coat_fp8_adamw_step_host(w, g, m_q, v_q, meta, G: int, beta1: float, beta2: 
     pmeta = _check_host(meta, torch.float32, 4 * num_groups(n, G), "meta")
     if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
         raise TypeError("workspace must be a contiguous CUDA tensor")
-    st = lib().coat_fp8_adamw_step_host(pw, pg, pm, pv, pmeta, n, int(G), float(beta1),
-                                        float(beta2), float(lr), float(eps), float(weight_decay),
-                                        int(step), workspace.data_ptr(),
-                                        workspace.numel() * workspace.element_size(),
-                                        _stream_ptr(stream))
+    with torch.cuda.device(workspace.device):
+        st = lib().coat_fp8_adamw_step_host(pw, pg, pm, pv, pmeta, n, int(G), float(beta1),
+                                            float(beta2), float(lr), float(eps),
+                                            float(weight_decay), int(step), workspace.data_ptr(),
+                                            workspace.numel() * workspace.element_size(),
+                                            _stream_ptr(stream))
     if st != 0:
         raise CoatError(st, "coat_fp8_adamw_step_host")
 
@@ -239,7 +243,8 @@ def coat_dre_quantize(x, G: int, q, scale, k, stream=None) -> None:
     pq = _check(q, torch.uint8, n, "q", x.device)
     ps = _check(scale, torch.float32, ng, "scale", x.device)
     pk = _check(k, torch.float32, ng, "k", x.device)
-    st = lib().coat_dre_quantize(px, n, int(G), pq, ps, pk, _stream_ptr(stream))
+    with torch.cuda.device(x.device):
+        st = lib().coat_dre_quantize(px, n, int(G), pq, ps, pk, _stream_ptr(stream))
     if st != 0:
         raise CoatError(st, "coat_dre_quantize")
 
@@ -253,7 +258,8 @@ def coat_fp8_quantize_absmax(x, G: int, q, scale, stream=None) -> None:
     px = _check(x, torch.float32, n, "x")
     pq = _check(q, torch.uint8, n, "q", x.device)
     ps = _check(scale, torch.float32, ng, "scale", x.device)
-    st = lib().coat_fp8_quantize_absmax(px, n, int(G), pq, ps, _stream_ptr(stream))
+    with torch.cuda.device(x.device):
+        st = lib().coat_fp8_quantize_absmax(px, n, int(G), pq, ps, _stream_ptr(stream))
     if st != 0:
         raise CoatError(st, "coat_fp8_quantize_absmax")
 
@@ -269,7 +275,8 @@ def coat_act_quantize_fp8(x, G: int, q, scale, qt=None, stream=None) -> None:
     pq = _check(q, torch.uint8, M * N, "q", x.device)
     ps = _check(scale, torch.float32, (M * N) // G if G > 0 else 0, "scale", x.device)
     pqt = _check(qt, torch.uint8, M * N, "qt", x.device) if qt is not None else None
-    st = lib().coat_act_quantize_fp8(px, M, N, int(G), pq, pqt, ps, _stream_ptr(stream))
+    with torch.cuda.device(x.device):
+        st = lib().coat_act_quantize_fp8(px, M, N, int(G), pq, pqt, ps, _stream_ptr(stream))
     if st != 0:
         raise CoatError(st, "coat_act_quantize_fp8")
 
@@ -283,6 +290,7 @@ def coat_dre_dequantize(q, scale, k, G: int, x, stream=None) -> None:
     ps = _check(scale, torch.float32, ng, "scale", q.device)
     pk = _check(k, torch.float32, ng, "k", q.device)
     px = _check(x, torch.float32, n, "x", q.device)
-    st = lib().coat_dre_dequantize(pq, ps, pk, n, int(G), px, _stream_ptr(stream))
+    with torch.cuda.device(q.device):
+        st = lib().coat_dre_dequantize(pq, ps, pk, n, int(G), px, _stream_ptr(stream))
     if st != 0:
         raise CoatError(st, "coat_dre_dequantize")

@@ -18,15 +18,23 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return a0 < b0 + nb && b0 < a0 + na;
 }
 
-// Device (or managed) memory of the current context.  Host memory is refused
-// even where the GPU could reach it, since the kernels assume HBM.
+// Device memory of the current device, or managed memory.  Host memory is
+// refused even where the GPU could reach it, since the kernels assume HBM,
+// and so is another device's memory: the kernels launch on the current one.
 bool is_device(const void* p) {
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
         cudaGetLastError();  // clear the sticky-free error state of this query
         return false;
     }
-    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+    if (at.type == cudaMemoryTypeManaged) return true;
+    if (at.type != cudaMemoryTypeDevice) return false;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.device == cur;
 }
 
 coat_status from_cuda(cudaError_t e) { return e == cudaSuccess ? COAT_OK : COAT_ERR_CUDA; }
