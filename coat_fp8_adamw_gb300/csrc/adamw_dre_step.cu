@@ -567,8 +567,22 @@ step_kernel_cta(const StepArgs a) {
     // A job may read a value another job of the same group has already
     // replaced by its exact value; the windows hold the exact values of the
     // true extremes too, so the outcome is the same.
+    // With 64 or more groups per CTA (G <= 32) the jobs run in blocks of NGC per
+    // statistic (max m, max v, min m, min v), so every job warp of a pass runs
+    // one kind of window test and the passes are balanced; with fewer groups a
+    // block would leave the minimum jobs to a single warp, and the jobs of a
+    // group stay on adjacent lanes instead.
+    constexpr bool kStatBlocks = NGC >= 64;
     for (int j = tid; j < 4 * NGC; j += kCta) {
-        const int jg = j >> 2, s = j & 3;
+        int jg, s;
+        if constexpr (kStatBlocks) {
+            const int blk = j / NGC;
+            jg = j - blk * NGC;
+            s = blk == 0 ? 0 : (blk == 1 ? 2 : (blk == 2 ? 1 : 3));
+        } else {
+            jg = j >> 2;
+            s = j & 3;
+        }
         GroupRec& r = grp[jg];
         const bool second = s >= 2, is_max = (s & 1) == 0;
         const int sm_ = second ? 1 : 0;
@@ -595,13 +609,68 @@ step_kernel_cta(const StepArgs a) {
                 cw[0] = cc.x; cw[1] = cc.y; cw[2] = cc.z; cw[3] = cc.w;
             }
             uint32_t msk = 0u;
+            if constexpr (kStatBlocks) {
+                // the window test of the job's statistic alone (`cand` without its
+                // inputs-live clause, which only decides for values exactly zero)
+                uint32_t zm = 0u;
+                if (is_max) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 x = *reinterpret_cast<const float4*>(vals + chunk_slot(th, q));
-                msk |= (cand(x.x, fabsf(bf16_of(gw, 4 * q)), byte_of(cw, 4 * q), ct) ? 1u : 0u) << (4 * q);
-                msk |= (cand(x.y, fabsf(bf16_of(gw, 4 * q + 1)), byte_of(cw, 4 * q + 1), ct) ? 1u : 0u) << (4 * q + 1);
-                msk |= (cand(x.z, fabsf(bf16_of(gw, 4 * q + 2)), byte_of(cw, 4 * q + 2), ct) ? 1u : 0u) << (4 * q + 2);
-                msk |= (cand(x.w, fabsf(bf16_of(gw, 4 * q + 3)), byte_of(cw, 4 * q + 3), ct) ? 1u : 0u) << (4 * q + 3);
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 x = *reinterpret_cast<const float4*>(vals + chunk_slot(th, q));
+                        msk |= ((fabsf(x.x) >= ct.hi ? 1u : 0u) | (fabsf(x.y) >= ct.hi ? 2u : 0u) |
+                                (fabsf(x.z) >= ct.hi ? 4u : 0u) | (fabsf(x.w) >= ct.hi ? 8u : 0u))
+                               << (4 * q);
+                    }
+                    if (!(ct.hi > 0.0f)) {   // a degenerate window admits zeros
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 x = *reinterpret_cast<const float4*>(vals + chunk_slot(th, q));
+                            zm |= ((x.x == 0.0f ? 1u : 0u) | (x.y == 0.0f ? 2u : 0u) |
+                                   (x.z == 0.0f ? 4u : 0u) | (x.w == 0.0f ? 8u : 0u)) << (4 * q);
+                        }
+                    }
+                } else if (second) {         // v: T_j = v_j, lo = max(a0, 0)
+                    const float lo = fmaxf(ct.a0, 0.0f);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 x = *reinterpret_cast<const float4*>(vals + chunk_slot(th, q));
+                        msk |= ((fabsf(x.x) <= lo ? 1u : 0u) | (fabsf(x.y) <= lo ? 2u : 0u) |
+                                (fabsf(x.z) <= lo ? 4u : 0u) | (fabsf(x.w) <= lo ? 8u : 0u)) << (4 * q);
+                        zm |= ((x.x == 0.0f ? 1u : 0u) | (x.y == 0.0f ? 2u : 0u) |
+                               (x.z == 0.0f ? 4u : 0u) | (x.w == 0.0f ? 8u : 0u)) << (4 * q);
+                    }
+                } else {                     // m: T_j = |m_j| + 2 (1 - beta1) |g_j|
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 x = *reinterpret_cast<const float4*>(vals + chunk_slot(th, q));
+                        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float ax = fabsf(xs[i]);
+                            const float Tj = fmaf(ct.c, fabsf(bf16_of(gw, 4 * q + i)), ax);
+                            const float lo = fmaxf(fmaf(ct.a1, Tj, ct.a0), ct.a2 * Tj);
+                            msk |= (ax <= lo ? 1u : 0u) << (4 * q + i);
+                            zm |= (ax == 0.0f ? 1u : 0u) << (4 * q + i);
+                        }
+                    }
+                }
+                // a value of exactly zero is a candidate only when its inputs are
+                // not both zero (the moment of zero inputs is exactly zero)
+                uint32_t zc = msk & zm;
+                while (zc) {
+                    const int e = __ffs(zc) - 1;
+                    zc &= zc - 1u;
+                    if (bf16_of(gw, e) == 0.0f && (byte_of(cw, e) & 0x7Fu) == 0u) msk &= ~(1u << e);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 x = *reinterpret_cast<const float4*>(vals + chunk_slot(th, q));
+                    msk |= (cand(x.x, fabsf(bf16_of(gw, 4 * q)), byte_of(cw, 4 * q), ct) ? 1u : 0u) << (4 * q);
+                    msk |= (cand(x.y, fabsf(bf16_of(gw, 4 * q + 1)), byte_of(cw, 4 * q + 1), ct) ? 1u : 0u) << (4 * q + 1);
+                    msk |= (cand(x.z, fabsf(bf16_of(gw, 4 * q + 2)), byte_of(cw, 4 * q + 2), ct) ? 1u : 0u) << (4 * q + 2);
+                    msk |= (cand(x.w, fabsf(bf16_of(gw, 4 * q + 3)), byte_of(cw, 4 * q + 3), ct) ? 1u : 0u) << (4 * q + 3);
+                }
             }
             while (msk) {
                 const int e = __ffs(msk) - 1;
