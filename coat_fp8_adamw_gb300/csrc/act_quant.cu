@@ -14,7 +14,9 @@
 // per thread and pass, statistics per thread and then across the G/8 lanes of
 // a group), store q and the scales, stage the codes in shared memory, and then
 // write qt as 16-byte runs of one column, each built from 4 x 4 byte
-// transposes.
+// transposes.  A thread keeps four passes' loads in flight at a time, which
+// holds it to 48 registers: ten CTAs per SM hide more latency than eight
+// passes of loads in flight in fewer CTAs.
 #include <cstdint>
 
 #include "coat_device.cuh"
@@ -70,7 +72,7 @@ constexpr int kActThreads = 128;
 constexpr int kPitchW = kTileC / 4 + 1;     // shared-memory row pitch in words (padded)
 
 template <int G>
-__global__ void __launch_bounds__(kActThreads)
+__global__ void __launch_bounds__(kActThreads, 10)
 act_quant_kernel(const ActArgs a) {
     __shared__ uint32_t tile[kTileR * kPitchW];
     const int tid = threadIdx.x;
@@ -82,17 +84,19 @@ act_quant_kernel(const ActArgs a) {
     const int r_in = tid >> 4;              // row within the pass
     const int c8 = (tid & 15) * 8;          // first column of this thread
     const bool col_ok = col0 + c8 < a.N;    // N % 16 == 0: all 8 columns or none
-    uint4 raw[kTileR / 8];
+    uint4 raw[kTileR / 16];
 #pragma unroll
     for (int p = 0; p < kTileR / 8; ++p) {
-        const int64_t r = row0 + 8 * p + r_in;
-        raw[p] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < a.M && col_ok) raw[p] = ld_cs(reinterpret_cast<const uint4*>(a.x + r * a.N + col0 + c8));
-    }
+        if ((p & 3) == 0) {   // four passes' loads in flight at a time
 #pragma unroll
-    for (int p = 0; p < kTileR / 8; ++p) {
+            for (int h = 0; h < 4; ++h) {
+                const int64_t rr = row0 + 8 * (p + h) + r_in;
+                raw[h] = make_uint4(0u, 0u, 0u, 0u);
+                if (rr < a.M && col_ok) raw[h] = ld_cs(reinterpret_cast<const uint4*>(a.x + rr * a.N + col0 + c8));
+            }
+        }
         const int64_t r = row0 + 8 * p + r_in;
-        const uint32_t w[4] = {raw[p].x, raw[p].y, raw[p].z, raw[p].w};
+        const uint32_t w[4] = {raw[p & 3].x, raw[p & 3].y, raw[p & 3].z, raw[p & 3].w};
         float x[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
