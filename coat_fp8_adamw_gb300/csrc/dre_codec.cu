@@ -21,8 +21,12 @@ struct Geom {
     static constexpr int kGpc = kJobs ? kThreads * kVec / G : 1;   // groups per CTA
 };
 
+// Eight 256-thread CTAs per SM for G >= 16 (32 registers, a few spilled):
+// with one group per thread the kernels are latency-bound and occupancy pays
+// more than the spills cost; below G = 16 a thread holds 16/G groups and the
+// register need grows with them.
 template <int G>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, G >= kVec ? 8 : 1)
 dre_quantize_kernel(const QuantArgs a) {
     using Gm = Geom<G>;
     __shared__ SmemTables st;
@@ -208,7 +212,7 @@ dre_dequantize_kernel(const DequantArgs a) {
 // quantization equation alone: S = max|X| / 448, q = RNE(X / S), saturating):
 // the reference point the expansion is measured against.
 template <int G>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, G >= kVec ? 8 : 1)
 absmax_quantize_kernel(const QuantArgs a) {
     using Gm = Geom<G>;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
