@@ -72,11 +72,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
     asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float sqrt_approx(float x) {
-    float y;
-    asm("sqrt.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 // Two fp32 values -> two E4M3 codes (round to nearest even, saturate to
 // +-448), packed little-endian: lo -> bits 0..7, hi -> bits 8..15.
@@ -85,9 +80,6 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return (uint32_t)r;
 }
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------------------
 // 128-bit streaming memory access (evict-first: the data set exceeds L2)
@@ -161,38 +153,6 @@ struct QuantParams {
     float inv_mx;  // 1/max (0 for an all-zero group)
 };
 
-__device__ __forceinline__ QuantParams quant_params(float mx, float mn) {
-    QuantParams q;
-    if (!(mx > 0.0f)) {
-        q.k = 1.0f;
-        q.S = 0.0f;
-        q.inv_mx = 0.0f;
-        return q;
-    }
-    float em, lm;
-    split_log2(mx, em, lm);
-    float k = 1.0f;
-    if (mn < mx) {
-        float en, ln;
-        split_log2(mn, en, ln);
-        const float D = (em - en) + (lm - ln);   // log2(R_X) > 0
-        k = fminf(__fdiv_rn(kLog2R, D), kKCap);
-    }
-    const float L = em + lm;                     // log2(max)
-    if (L < 0.0f)
-        k = fminf(k, __fdiv_rn(kGuardLo, L));
-    else if (L > 0.0f)
-        k = fminf(k, __fdiv_rn(kGuardHi, L));
-    // S = 2^(k em + k lm - log2 448), with k*em split exactly
-    const float p = __fmul_rn(k, em);
-    const float pe = fmaf(k, em, -p);
-    const float slo = fmaf(k, lm, pe) - kLog2_448;
-    q.k = k;
-    q.S = exp2_split(p, slo);
-    q.inv_mx = __frcp_rn(mx);
-    return q;
-}
-
 // Shared-memory copy of the double-float tables (divergent indices: constant
 // memory would serialize them).
 struct SmemTables {
@@ -263,11 +223,6 @@ __device__ __forceinline__ float dequant_one(const float* s_log_tab, uint32_t co
 __device__ __forceinline__ float expand_scaled(float x, float r, float k) {
     const float y = ex2_approx(fmaf(k, lg2_approx(r), kLog2_448));
     return __fadd_rn(copysignf(y, x), 0.0f);
-}
-
-// Same for a non-negative value (the second moment): no sign to carry.
-__device__ __forceinline__ float expand_scaled_pos(float r, float k) {
-    return ex2_approx(fmaf(k, lg2_approx(r), kLog2_448));
 }
 
 // x / S ready for an E4M3 round-to-nearest-even conversion that rounds the
