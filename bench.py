@@ -38,7 +38,7 @@ L2_BYTES = 129 * 2 ** 20
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default="llama7b")
     p.add_argument("--G", type=int, default=128)
