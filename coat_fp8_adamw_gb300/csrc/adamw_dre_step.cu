@@ -78,8 +78,9 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kStepCta = COAT_STEP_CTA;    // threads per CTA of the step kernel
 #define kInf __int_as_float(0x7F800000)
 
-// Relative error bound of the SFU exp2 (ex2.approx.ftz.f32), with margin.
-constexpr float kEx2Err = 4.76837158203125e-07f;   // 2^-21
+// Relative error bound of the SFU exp2 (ex2.approx.ftz.f32) for normal
+// results; an exhaustive check over the arguments used here stays below it.
+constexpr float kEx2Err = 2.384185791015625e-07f;   // 2^-22
 
 // Bound on the relative error of a fast dequantized moment of a group whose
 // stored exponent is k (1/k = rk): the SFU exp2 of the factor P and of the
