@@ -492,8 +492,7 @@ step_kernel_cta(const StepArgs a) {
         const float Pm = r.P[0], rkm = r.rkd[0].hi, rkv = r.rkd[1].hi;
         const float bPm = a.beta1 * Pm, bPv = a.beta2 * r.P[1];
         float lmx_m = 0.0f, lmx_v = 0.0f, lmx_g = 0.0f;
-        float lmn_m = kInf, lmn_v = kInf;   // smallest non-zero, as keys
-        float lz = kInf;                    // smallest |m| or v, zeros included
+        float lmn_m = kInf, lmn_v = kInf;   // smallest |m| and v, zeros included
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float mt[4], vt[4];
@@ -506,10 +505,8 @@ step_kernel_cta(const StepArgs a) {
             lmx_g = fmax3(fmax3(lmx_g, fabsf(g0), fabsf(g1)), fabsf(g2), fabsf(g3));
             lmx_m = fmax3(fmax3(lmx_m, fabsf(mt[0]), fabsf(mt[1])), fabsf(mt[2]), fabsf(mt[3]));
             lmx_v = fmax3(fmax3(lmx_v, vt[0], vt[1]), vt[2], vt[3]);
-            lmn_m = fmin3(fmin3(lmn_m, nz_key(mt[0]), nz_key(mt[1])), nz_key(mt[2]), nz_key(mt[3]));
-            lmn_v = fmin3(fmin3(lmn_v, nz_key(vt[0]), nz_key(vt[1])), nz_key(vt[2]), nz_key(vt[3]));
-            lz = fmin3(fmin3(lz, fabsf(mt[0]), fabsf(mt[1])), fabsf(mt[2]), fabsf(mt[3]));
-            lz = fmin3(fmin3(lz, vt[0], vt[1]), vt[2], vt[3]);
+            lmn_m = fmin3(fmin3(lmn_m, fabsf(mt[0]), fabsf(mt[1])), fabsf(mt[2]), fabsf(mt[3]));
+            lmn_v = fmin3(fmin3(lmn_v, vt[0], vt[1]), vt[2], vt[3]);
             const int slot = chunk_slot(tid, q);
             *reinterpret_cast<float4*>(&sm_m[tid][slot]) = make_float4(mt[0], mt[1], mt[2], mt[3]);
             *reinterpret_cast<float4*>(&sm_v[tid][slot]) = make_float4(vt[0], vt[1], vt[2], vt[3]);
@@ -520,6 +517,22 @@ step_kernel_cta(const StepArgs a) {
         sm_in[4 * tid + 1] = make_uint4(c.g[4], c.g[5], c.g[6], c.g[7]);
         sm_in[4 * tid + 2] = make_uint4(c.mq[0], c.mq[1], c.mq[2], c.mq[3]);
         sm_in[4 * tid + 3] = make_uint4(c.vq[0], c.vq[1], c.vq[2], c.vq[3]);
+
+        // smallest non-zero values as keys; a lane holding an exact zero (rare:
+        // both inputs of an element zero, or a fast sum that cancels) rescans
+        // its values
+        const float lz = fminf(lmn_m, lmn_v);   // zero iff a fast value is zero
+        lmn_m = nz_key(lmn_m);
+        lmn_v = nz_key(lmn_v);
+        if (lz == 0.0f) {
+            lmn_m = kInf;
+            lmn_v = kInf;
+#pragma unroll 1
+            for (int e = 0; e < kVec; ++e) {
+                lmn_m = fminf(lmn_m, nz_key(sm_m[tid][e]));
+                lmn_v = fminf(lmn_v, nz_key(sm_v[tid][e]));
+            }
+        }
 
         // stage 2 across the lanes of the group
         float fmx_m = lmx_m, fmx_v = lmx_v, gmx = lmx_g, fmn_m = lmn_m, fmn_v = lmn_v;
