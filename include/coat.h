@@ -65,7 +65,7 @@ typedef enum {
     COAT_ERR_MISALIGNED = 2,    /* a pointer is not 16-byte aligned */
     COAT_ERR_UNSUPPORTED_G = 3, /* G not a power of two in [1, 256] */
     COAT_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
-    COAT_ERR_NOT_DEVICE = 5,    /* a pointer is not memory of the current device (or managed) */
+    COAT_ERR_NOT_DEVICE = 5,    /* a device pointer is neither memory of the current device nor managed memory */
     COAT_ERR_SCRATCH_LIMIT = 6  /* the request needs more than COAT_STATIC_SCRATCH_BYTES */
 } coat_status;
 
