@@ -1,6 +1,7 @@
 """The relative error of the SFU exp2 (PTX ex2.approx.ftz.f32) that the step
-kernel's fast-path error bound assumes: at most 2^-22 for every fp32 input
-whose result is a normal float, over the arguments the fast path gives it
+kernel's fast-path error bound assumes (its constant kEx2Err, read from the
+kernel source): no larger than that for every fp32 input whose result is a
+normal float, over the arguments the fast path gives it
 (the fractional part of a scale exponent, and L(q)/k <= 0 for a stored code).
 
 The check is exhaustive: a small probe, compiled here with nvcc, evaluates
@@ -11,13 +12,15 @@ double-precision exp2 of the same input.  The open end stops one float above
 import ctypes
 import math
 import os
+import re
 import shutil
 import struct
 import subprocess
 
 import pytest
 
-pytestmark = pytest.mark.gpu
+STEP_SRC = os.path.join(os.path.dirname(__file__), "..", "coat_fp8_adamw_gb300", "csrc",
+                        "adamw_dre_step.cu")
 
 PROBE = r"""
 #include <cstdint>
@@ -66,7 +69,21 @@ def _f32_bits(v):
     return struct.unpack("<I", struct.pack("<f", v))[0]
 
 
-def test_ex2_approx_ftz_relative_error_below_2_pow_minus_22(tmp_path):
+def kernel_ex2_bound() -> float:
+    """The bound the step kernel's fast path assumes for the SFU exp2."""
+    with open(STEP_SRC) as fh:
+        m = re.search(r"constexpr float kEx2Err = ([0-9.eE+-]+)f;", fh.read())
+    assert m, "kEx2Err not found in the step kernel source"
+    return float(m.group(1))
+
+
+def test_kernel_bound_is_a_power_of_two():
+    b = kernel_ex2_bound()
+    assert math.frexp(b)[0] == 0.5 and 2.0 ** -24 < b <= 2.0 ** -21
+
+
+@pytest.mark.gpu
+def test_ex2_approx_ftz_relative_error_within_kernel_bound(tmp_path):
     nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     if not os.path.exists(nvcc):
         pytest.skip("nvcc not found")
@@ -84,5 +101,7 @@ def test_ex2_approx_ftz_relative_error_below_2_pow_minus_22(tmp_path):
     worst_neg = L.max_rel_err(0x80000000, _f32_bits(-126.0) - 1)
     assert worst_pos >= 0.0 and worst_neg >= 0.0, "the probe failed to run"
     worst = max(worst_pos, worst_neg)
-    print("max relative error of ex2.approx.ftz.f32: 2^%.3f" % math.log2(worst))
-    assert worst <= 2.0 ** -22
+    bound = kernel_ex2_bound()
+    print("max relative error of ex2.approx.ftz.f32: 2^%.3f (bound 2^%g)"
+          % (math.log2(worst), math.log2(bound)))
+    assert worst <= bound
