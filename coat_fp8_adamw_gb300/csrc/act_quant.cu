@@ -1,8 +1,9 @@
 // act_quant.cu -- per-group (1 x G) FP8 quantization of an activation tensor
-// with a transposed FP8 second output (COAT review page, section 4,
-// "non-linear layer optimisation": quantized FP8 output plus a transposed FP8
-// output for the backward pass; groups along the last dimension with a
-// two-stage maximum reduction).
+// with a transposed FP8 second output (COAT review page: section 3, Triton
+// kernels, "non-linear layer optimisation": quantized FP8 output plus a
+// transposed FP8 output for the backward pass; section 3, mixed-granularity
+// activation quantization: 1 x G groups for non-linear layers; section 4
+// table, group-scaling row: two-stage maximum reduction).
 //
 // x is an M x N bf16 tensor in row-major order.  Each row is split into
 // groups of G consecutive elements; a group's scale is S = max|x| / 448 and its

@@ -201,10 +201,12 @@ coat_status coat_fp8_quantize_absmax(const float *x, int64_t n, int32_t G, uint8
 
 /*
  * Per-group (1 x G) FP8 quantization of an activation with a transposed FP8
- * second output (COAT review page, section 4, "non-linear layer optimisation":
- * a quantized FP8 output plus a transposed FP8 output for the backward pass,
- * groups along the last dimension, two-stage maximum; the section 5 group-size
- * table sweeps G = 4 ... 64 and 1 x 128).  Each row of x is split into groups
+ * second output (COAT review page: section 3, Triton kernels, "non-linear
+ * layer optimisation": a quantized FP8 output plus a transposed FP8 output for
+ * the backward pass; section 3, mixed-granularity activation quantization:
+ * 1 x G groups for non-linear layers; section 4 table, group-scaling row:
+ * two-stage maximum; the section 5 group-size table sweeps G = 4 ... 64 and
+ * 1 x 128).  Each row of x is split into groups
  * of G consecutive elements: scale = max|x| / 448 rounded to float, and
  * q = E4M3(x / scale) rounded to nearest even, saturating; an all-zero group
  * has scale 0 and zero codes.

@@ -199,6 +199,40 @@ def act_quantize(x_bf16_bits: np.ndarray, G: int, nthreads: int = 0):
     return q, np.ascontiguousarray(q.T), S.reshape(M, N // G)
 
 
+def linear_group_quantize(xq: np.ndarray, sx: float, wq: np.ndarray, sw: float, G: int,
+                          nthreads: int = 0):
+    """FP8 linear layer with a per-group FP8 output -> (y [M, N] float32,
+    q [M, N] uint8, S [M, N/G] float32).
+
+    The inputs are quantized per tensor, as the page's mixed-granularity
+    scheme has it for linear layers (section 3, "mixed-granularity activation
+    quantization", and the section 4 table's row of that name): X = sx
+    E4M3(xq) with xq [M, K], W = sw E4M3(wq) with wq [N, K].  y = X W^T,
+    rounded once to float32 (the ideal fp32 accumulator).  The output is then
+    quantized per 1 x G group along each row, as :func:`absmax_quantize` does
+    (section 3, "Triton kernels", linear layer optimisation: the output tile
+    is reshaped to (BLOCK_M, BLOCK_N/G, G) and the maximum taken along the
+    last axis).
+
+    The sum over K is exact in float64 for K <= 2^17: every E4M3 value is an
+    integer multiple of 2^-9 below 2^9, so every product is a multiple of
+    2^-18 below 2^18.  sx sw is exact in float64 too; the one float64 rounding
+    of (sx sw) times the sum, before the float32 rounding, can only matter
+    when it lands exactly on a float32 midpoint.
+    """
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    M, K = xq.shape
+    N, K2 = wq.shape
+    if K != K2 or N % G or K > (1 << 17):
+        raise ValueError("oracle linear_group_quantize: bad shapes")
+    dec = e4m3_decode_all()
+    acc = dec[xq] @ dec[wq].T                        # exact (see above)
+    y = ((np.float64(np.float32(sx)) * np.float64(np.float32(sw))) * acc).astype(np.float32)
+    q, S = absmax_quantize(y, G, nthreads)
+    return y, q.reshape(M, N), S.reshape(M, N // G)
+
+
 def dre_dequantize(q: np.ndarray, S: np.ndarray, k: np.ndarray, G: int,
                    nthreads: int = 0) -> np.ndarray:
     """Inverse of :func:`dre_quantize`: sign(q) (|dec(q)| S)^(1/k) rounded to fp32."""
