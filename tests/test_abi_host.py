@@ -1,6 +1,5 @@
 """The C-ABI library loads, exports every declared symbol, and validates
 arguments on the host (CPU only: no call here reaches a kernel)."""
-import ctypes
 import os
 import re
 
