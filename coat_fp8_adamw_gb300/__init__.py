@@ -23,7 +23,7 @@ __all__ = ["CoatError", "coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
            "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_act_quantize_fp8",
            "coat_dre_dequantize", "coat_status_string", "coat_r_e4m3", "coat_version", "lib",
            "lib_path", "num_groups", "bytes_per_param", "STATUS",
-           "STATIC_SCRATCH_BYTES"]
+           "STATIC_SCRATCH_BYTES", "MAX_N"]
 
 STATUS = {0: "COAT_OK", 1: "COAT_ERR_INVALID_ARG", 2: "COAT_ERR_MISALIGNED",
           3: "COAT_ERR_UNSUPPORTED_G", 4: "COAT_ERR_CUDA", 5: "COAT_ERR_NOT_DEVICE",
@@ -31,6 +31,9 @@ STATUS = {0: "COAT_OK", 1: "COAT_ERR_INVALID_ARG", 2: "COAT_ERR_MISALIGNED",
 
 #: COAT_STATIC_SCRATCH_BYTES of include/coat.h
 STATIC_SCRATCH_BYTES = 16 << 20
+
+#: COAT_MAX_N of include/coat.h: the largest element count any entry point accepts
+MAX_N = 1 << 40
 
 #: symbols the shared library must export (one per declaration in include/coat.h)
 EXPORTS = ("coat_fp8_adamw_step", "coat_fp8_adamw_step_host",

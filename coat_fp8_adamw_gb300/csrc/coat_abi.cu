@@ -11,6 +11,7 @@
 namespace {
 
 bool pow2_group(int32_t G) { return G >= 1 && G <= 256 && (G & (G - 1)) == 0; }
+bool size_ok(int64_t n) { return n >= 1 && n <= COAT_MAX_N; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -52,7 +53,7 @@ coat_status check_step_args(const float* w, const uint16_t* g, const uint8_t* m_
                             const uint8_t* v_q, const coat_group_meta* meta, int64_t n, int32_t G,
                             float beta1, float beta2, float lr, float eps, float weight_decay,
                             int64_t step) {
-    if (!w || !g || !m_q || !v_q || !meta || n < 1 || step < 1) return COAT_ERR_INVALID_ARG;
+    if (!w || !g || !m_q || !v_q || !meta || !size_ok(n) || step < 1) return COAT_ERR_INVALID_ARG;
     if (!pow2_group(G)) return COAT_ERR_UNSUPPORTED_G;
     if (!aligned16(w) || !aligned16(g) || !aligned16(m_q) || !aligned16(v_q) || !aligned16(meta))
         return COAT_ERR_MISALIGNED;
@@ -117,7 +118,7 @@ coat_status coat_fp8_adamw_step(float* w, const uint16_t* g, uint8_t* m_q, uint8
 
 coat_status coat_dre_quantize(const float* x, int64_t n, int32_t G, uint8_t* q, float* scale,
                               float* k, void* stream) {
-    if (!x || !q || !scale || !k || n < 1) return COAT_ERR_INVALID_ARG;
+    if (!x || !q || !scale || !k || !size_ok(n)) return COAT_ERR_INVALID_ARG;
     if (!pow2_group(G)) return COAT_ERR_UNSUPPORTED_G;
     if (!aligned16(x) || !aligned16(q) || !aligned16(scale) || !aligned16(k))
         return COAT_ERR_MISALIGNED;
@@ -134,7 +135,7 @@ coat_status coat_dre_quantize(const float* x, int64_t n, int32_t G, uint8_t* q, 
 
 coat_status coat_fp8_quantize_absmax(const float* x, int64_t n, int32_t G, uint8_t* q, float* scale,
                                      void* stream) {
-    if (!x || !q || !scale || n < 1) return COAT_ERR_INVALID_ARG;
+    if (!x || !q || !scale || !size_ok(n)) return COAT_ERR_INVALID_ARG;
     if (!pow2_group(G)) return COAT_ERR_UNSUPPORTED_G;
     if (!aligned16(x) || !aligned16(q) || !aligned16(scale)) return COAT_ERR_MISALIGNED;
     const size_t nb = (size_t)n, ng = (size_t)num_groups(n, G);
@@ -167,7 +168,7 @@ coat_status coat_act_quantize_fp8(const uint16_t* x, int64_t M, int64_t N, int32
 
 coat_status coat_dre_dequantize(const uint8_t* q, const float* scale, const float* k, int64_t n,
                                 int32_t G, float* x, void* stream) {
-    if (!x || !q || !scale || !k || n < 1) return COAT_ERR_INVALID_ARG;
+    if (!x || !q || !scale || !k || !size_ok(n)) return COAT_ERR_INVALID_ARG;
     if (!pow2_group(G)) return COAT_ERR_UNSUPPORTED_G;
     if (!aligned16(x) || !aligned16(q) || !aligned16(scale) || !aligned16(k))
         return COAT_ERR_MISALIGNED;
@@ -196,6 +197,6 @@ const char* coat_status_string(coat_status s) {
 
 double coat_r_e4m3(void) { return 448.0 * 512.0; }
 
-int32_t coat_version(void) { return 100; }
+int32_t coat_version(void) { return 101; }
 
 }  // extern "C"

@@ -42,7 +42,9 @@
  *     stream).  Every call is asynchronous on that stream, except
  *     coat_fp8_adamw_step_host and coat_fp8_adamw_step_host_static, which
  *     return when their result is in host memory.
- *   - G must be a power of two in [1, 256]; n >= 1.
+ *   - G must be a power of two in [1, 256]; 1 <= n <= COAT_MAX_N (2^40
+ *     elements: far more than one device holds, and small enough that every
+ *     launch's grid stays within the hardware's limits).
  *   - Argument errors return a status and launch nothing.  A failed launch
  *     returns COAT_ERR_CUDA (the CUDA error is left for the caller to query
  *     with cudaGetLastError()).  Nothing aborts, traps or prints.
@@ -61,13 +63,16 @@ extern "C" {
 
 typedef enum {
     COAT_OK = 0,
-    COAT_ERR_INVALID_ARG = 1,   /* null pointer, n < 1, step < 1, bad hyper-parameter, aliasing */
+    COAT_ERR_INVALID_ARG = 1,   /* null pointer, n outside [1, COAT_MAX_N], step < 1, bad hyper-parameter, aliasing */
     COAT_ERR_MISALIGNED = 2,    /* a pointer is not 16-byte aligned */
     COAT_ERR_UNSUPPORTED_G = 3, /* G not a power of two in [1, 256] */
     COAT_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
     COAT_ERR_NOT_DEVICE = 5,    /* a device pointer is neither memory of the current device nor managed memory */
     COAT_ERR_SCRATCH_LIMIT = 6  /* the request needs more than COAT_STATIC_SCRATCH_BYTES */
 } coat_status;
+
+/* Largest element count n any entry point accepts. */
+#define COAT_MAX_N ((int64_t)1 << 40)
 
 /* Size of the fixed device scratch buffer of coat_fp8_adamw_step_host_static. */
 #define COAT_STATIC_SCRATCH_BYTES ((size_t)16 << 20)

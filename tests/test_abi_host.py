@@ -65,6 +65,25 @@ def test_step_validation(L):
     assert _step(L) == 5
 
 
+def test_header_constants_match_the_binding():
+    src = open(os.path.join(ROOT, "include", "coat.h")).read()
+    assert re.search(r"#define COAT_MAX_N \(\(int64_t\)1 << 40\)", src)
+    assert re.search(r"#define COAT_STATIC_SCRATCH_BYTES \(\(size_t\)16 << 20\)", src)
+    assert coat.MAX_N == 1 << 40 and coat.STATIC_SCRATCH_BYTES == 16 << 20
+
+
+def test_sizes_beyond_the_limit_are_refused(L):
+    big = coat.MAX_N + 1
+    assert _step(L, n=big) == 1
+    assert _static(L, n=big) == 1
+    assert L.coat_dre_quantize(A, big, 16, A + 4096, A + 8192, A + 12288, None) == 1
+    assert L.coat_fp8_quantize_absmax(A, big, 16, A + 4096, A + 8192, None) == 1
+    assert L.coat_dre_dequantize(A, A + 4096, A + 8192, big, 16, A + 12288, None) == 1
+    assert L.coat_fp8_adamw_step_host(A, A + 0x100000, A + 0x200000, A + 0x300000, A + 0x400000,
+                                      big, 128, 0.9, 0.95, 1e-4, 1e-8, 0.1, 1, A + 0x500000,
+                                      1 << 20, None) == 1
+
+
 def test_codec_validation(L):
     assert L.coat_dre_quantize(0, 16, 16, A, A + 4096, A + 8192, None) == 1
     assert L.coat_dre_quantize(A, 16, 7, A + 4096, A + 8192, A + 12288, None) == 3
