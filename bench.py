@@ -163,7 +163,9 @@ def measured_peak():
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "coat_fp8_adamw_gb300", "csrc")
-    for name in ("adamw_dre_step.cu", "coat_device.cuh", "coat_tables.inc"):
+    # every file the step kernel is compiled from (the C ABI header only declares)
+    for name in ("adamw_dre_step.cu", "coat_device.cuh", "coat_df.cuh", "coat_tables.inc",
+                 "coat_kernels.h"):
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
