@@ -25,7 +25,7 @@ import oracle
 from coat_fp8_adamw_gb300 import synth
 
 import _parity as P
-from test_gpu_sfu_bound import kernel_ex2_bound
+from _kernel_consts import kernel_ex2_bound
 
 F = np.float32
 KERNEL_EX2_ERR = kernel_ex2_bound()   # the SFU bound the kernel's fast_err budgets

@@ -12,15 +12,13 @@ double-precision exp2 of the same input.  The open end stops one float above
 import ctypes
 import math
 import os
-import re
 import shutil
 import struct
 import subprocess
 
 import pytest
 
-STEP_SRC = os.path.join(os.path.dirname(__file__), "..", "coat_fp8_adamw_gb300", "csrc",
-                        "adamw_dre_step.cu")
+from _kernel_consts import kernel_ex2_bound
 
 PROBE = r"""
 #include <cstdint>
@@ -67,14 +65,6 @@ extern "C" double max_rel_err(uint32_t b0, uint32_t b1) {
 
 def _f32_bits(v):
     return struct.unpack("<I", struct.pack("<f", v))[0]
-
-
-def kernel_ex2_bound() -> float:
-    """The bound the step kernel's fast path assumes for the SFU exp2."""
-    with open(STEP_SRC) as fh:
-        m = re.search(r"constexpr float kEx2Err = ([0-9.eE+-]+)f;", fh.read())
-    assert m, "kEx2Err not found in the step kernel source"
-    return float(m.group(1))
 
 
 def test_kernel_bound_is_a_power_of_two():
