@@ -56,3 +56,37 @@ def test_near_midpoint_values_round_correctly():
         got = oracle.dre_dequantize(codes[idx:idx + 1], S[idx:idx + 1], k[idx:idx + 1], G)[0]
         want = _correct_fp32(int(codes[idx]), S[idx], k[idx], dec)
         assert got == want, (int(codes[idx]), float(S[idx]), float(k[idx]))
+
+
+def _correct_k(mx, mn):
+    """k = log R_E4M3 / log(max/min), below the cap, correctly rounded to fp32."""
+    x = mpmath.log(mpmath.mpf(229376)) / mpmath.log(mpmath.mpf(float(mx)) / mpmath.mpf(float(mn)))
+    f = np.float32(float(x))
+    e = np.frexp(f)[1] - 24
+    u = mpmath.ldexp(1, int(e))
+    q = x / u
+    n = mpmath.floor(q)
+    r = q - n
+    if r > 0.5 or (r == 0.5 and int(n) % 2 == 1):
+        n += 1
+    return np.float32(float(n * u))
+
+
+def test_k_near_midpoints_rounds_correctly():
+    rng = np.random.default_rng(32)
+    N = 4_000_000
+    mx = np.exp2(rng.uniform(-30.0, -2.0, N)).astype(np.float32)
+    mn = (mx.astype(np.float64) * np.exp2(-rng.uniform(2.5, 40.0, N))).astype(np.float32)
+    k = np.log(229376.0) / np.log(mx.astype(np.float64) / mn.astype(np.float64))
+    ulp = np.spacing(k.astype(np.float32)).astype(np.float64)
+    frac = k / ulp
+    dist = np.abs(frac - np.floor(frac) - 0.5)
+    # below the cap, and below the S-range guard's bound (S = max^k / 448 >= 2^-125)
+    guard = (np.log2(448.0) - 125.0) / np.log2(mx.astype(np.float64))
+    free = (k < 7.9) & (k < guard * (1 - 1e-6))
+    hard = np.nonzero(free & (dist < 1e-5))[0][:40]
+    assert hard.size >= 20, "the search found too few values of k near a midpoint"
+    for idx in np.concatenate([hard, np.nonzero(free)[0][:20]]):
+        group = np.array([mx[idx], mn[idx]], np.float32)
+        got = oracle.dre_group(group)["k"]
+        assert np.float32(got) == _correct_k(mx[idx], mn[idx]), (float(mx[idx]), float(mn[idx]))
