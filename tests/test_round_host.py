@@ -44,3 +44,48 @@ def test_header_compiles_for_the_device(tmp_path):
         "}\n")
     subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-std=c++17", "-I", CSRC,
                     "-c", str(src), "-o", str(tmp_path / "use_round.o")], check=True)
+
+
+def test_float64_recomputations_match_the_oracle(tmp_path):
+    """The recomputations reproduce the oracle's definitions: its dequantized
+    moments, and its k with the cap and the S-range guard, for groups of two
+    magnitudes (max, min) spread over the whole range."""
+    import ctypes
+
+    import numpy as np
+
+    import oracle
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    src = tmp_path / "f64.cpp"
+    src.write_text('#include "coat_round.cuh"\n'
+                   'extern "C" float dq(float m, float s, float k) { return coat::df::dequant_f64(m, s, k); }\n'
+                   'extern "C" float kk(float mx, float mn) {\n'
+                   '    return coat::df::k_f64(mx, mn, 229376.0, 8.0, -125.0, 126.0); }\n')
+    lib = tmp_path / "libf64.so"
+    subprocess.run([cxx, "-O2", "-std=c++17", "-ffp-contract=off", "-shared", "-fPIC", "-I", CSRC,
+                    str(src), "-o", str(lib)], check=True)
+    L = ctypes.CDLL(str(lib))
+    L.dq.argtypes = [ctypes.c_float] * 3
+    L.dq.restype = ctypes.c_float
+    L.kk.argtypes = [ctypes.c_float] * 2
+    L.kk.restype = ctypes.c_float
+    rng = np.random.default_rng(33)
+    dec = oracle.e4m3_decode_all()
+    codes = rng.choice(np.array([c for c in range(1, 127) if c != 0x7F], np.uint8), 3000)
+    S = np.exp2(rng.uniform(-120.0, 0.0, codes.size)).astype(np.float32)
+    k = rng.uniform(0.6, 8.0, codes.size).astype(np.float32)
+    for c, s, kv in zip(codes, S, k):
+        want = oracle.dre_dequantize(np.array([c], np.uint8), np.array([s]), np.array([kv]), 1)[0]
+        assert np.float32(L.dq(float(dec[c]), float(s), float(kv))) == want
+    # (max, min) pairs: ordinary, capped (ratio below 4.68), guard-active (tiny or huge max)
+    lmx = rng.uniform(-140.0, 120.0, 3000)
+    ratio = np.where(rng.random(3000) < 0.2, rng.uniform(0.0, 2.2, 3000), rng.uniform(2.2, 40.0, 3000))
+    for a, r in zip(lmx, ratio):
+        mx = np.float32(2.0 ** a)
+        mn = np.float32(2.0 ** (a - r))
+        if not (mn > 0 and np.isfinite(mx)):
+            continue
+        g = oracle.dre_group(np.array([mx, mn], np.float32))
+        assert np.float32(L.kk(float(mx), float(mn))) == np.float32(g["k"]), (float(mx), float(mn))
