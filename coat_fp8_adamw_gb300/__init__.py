@@ -21,7 +21,8 @@ from . import _build
 __all__ = ["CoatError", "coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
            "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
            "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_act_quantize_fp8",
-           "coat_dre_dequantize", "coat_status_string", "coat_r_e4m3", "coat_version", "lib",
+           "coat_dre_dequantize", "coat_exact_recompute_counts", "coat_status_string",
+           "coat_r_e4m3", "coat_version", "lib",
            "lib_path", "num_groups", "bytes_per_param", "STATUS",
            "STATIC_SCRATCH_BYTES", "MAX_N"]
 
@@ -39,7 +40,8 @@ MAX_N = 1 << 40
 EXPORTS = ("coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
            "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
            "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_act_quantize_fp8",
-           "coat_dre_dequantize", "coat_status_string", "coat_r_e4m3", "coat_version")
+           "coat_dre_dequantize", "coat_exact_recompute_counts", "coat_status_string",
+           "coat_r_e4m3", "coat_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -88,6 +90,8 @@ def lib() -> ctypes.CDLL:
         L.coat_act_quantize_fp8.restype = ctypes.c_int
         L.coat_dre_dequantize.argtypes = [vp, vp, vp, i64, i32, vp, vp]
         L.coat_dre_dequantize.restype = ctypes.c_int
+        L.coat_exact_recompute_counts.argtypes = [vp, i32]
+        L.coat_exact_recompute_counts.restype = ctypes.c_int
         L.coat_status_string.argtypes = [ctypes.c_int]
         L.coat_status_string.restype = ctypes.c_char_p
         L.coat_r_e4m3.argtypes = []
@@ -96,6 +100,20 @@ def lib() -> ctypes.CDLL:
         L.coat_version.restype = ctypes.c_int32
         _lib = L
         return L
+
+
+def coat_exact_recompute_counts(reset: bool = False, device=None) -> tuple:
+    """(dequantized moments, exponents k) that the step's exact path recomputed
+    in float64 on ``device`` (default: the current one) since load or the last
+    reset.  Synchronizes with that device."""
+    import torch
+    out = (ctypes.c_uint64 * 2)()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        st = lib().coat_exact_recompute_counts(ctypes.cast(out, ctypes.c_void_p), int(bool(reset)))
+    if st != 0:
+        raise CoatError(st, "coat_exact_recompute_counts")
+    return int(out[0]), int(out[1])
 
 
 def coat_status_string(status: int) -> str:
@@ -229,10 +247,14 @@ def coat_fp8_adamw_step_host_static(w, g, m_q, v_q, meta, G: int, beta1: float, 
     pm = _check_host(m_q, torch.uint8, n, "m_q")
     pv = _check_host(v_q, torch.uint8, n, "v_q")
     pmeta = _check_host(meta, torch.float32, 4 * num_groups(n, G), "meta")
-    st = lib().coat_fp8_adamw_step_host_static(pw, pg, pm, pv, pmeta, n, int(G), float(beta1),
-                                               float(beta2), float(lr), float(eps),
-                                               float(weight_decay), int(step), int(chunk_params),
-                                               _stream_ptr(stream))
+    # the call runs on the stream's device (the current one when no stream is given)
+    dev = stream.device if isinstance(stream, torch.cuda.Stream) else torch.device(
+        "cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        st = lib().coat_fp8_adamw_step_host_static(pw, pg, pm, pv, pmeta, n, int(G), float(beta1),
+                                                   float(beta2), float(lr), float(eps),
+                                                   float(weight_decay), int(step),
+                                                   int(chunk_params), _stream_ptr(stream, dev))
     if st != 0:
         raise CoatError(st, "coat_fp8_adamw_step_host_static")
 

@@ -46,8 +46,14 @@
 
 #include "coat_device.cuh"
 #include "coat_kernels.h"
+#include "coat_round.cuh"
 
 namespace coat {
+
+// How often the exact path fell back to float64 because a double-float value
+// lay too close to an fp32 rounding midpoint to round with certainty:
+// [0] dequantized moments, [1] exponents k.  Only the rare path touches them.
+__device__ unsigned long long g_recompute[2];
 
 // The tables of the exact path, in global memory: only the few lanes that
 // re-evaluate candidates (and the per-group jobs) read them, through L1, so
@@ -201,8 +207,10 @@ __device__ __forceinline__ StateParams state_params(float S, float k, const df::
 // with x = g (first moment) or g^2 (second moment, exact for a bf16 g).
 // For k = 1 the power is the plain product |E4M3(q)| S, which is often a
 // rounding tie: it is formed by one correctly rounded multiplication.
+// Otherwise the power is rounded with certainty (float64 in the rare case
+// where the double-float value lies too near an fp32 rounding midpoint).
 __device__ __forceinline__ float exact_moment(uint32_t code, float gf, bool second, F2 A, F2 rkd,
-                                              float S, float beta, float omb,
+                                              float S, float k, float beta, float omb,
                                               const df::Tables& t, const float* lg_hi,
                                               const float* lg_lo) {
     float prev = 0.0f;
@@ -212,7 +220,9 @@ __device__ __forceinline__ float exact_moment(uint32_t code, float gf, bool seco
             prev = __fmul_rn(e4m3_value(mag), S);
         } else {
             const F2 L = {lg_hi[mag], lg_lo[mag]};
-            prev = df::exp2_df(df::mul22(df::add2(L, A), rkd), t);
+            bool slow = false;
+            prev = df::dequant_certain(L, A, rkd, e4m3_value(mag), S, k, t, slow);
+            if (slow) atomicAdd(&g_recompute[0], 1ull);
         }
         if (code & 0x80u) prev = -prev;
     }
@@ -220,8 +230,23 @@ __device__ __forceinline__ float exact_moment(uint32_t code, float gf, bool seco
     return df::dot2_rn(beta, prev, omb, x);
 }
 
-// k rounded once from double-float logs of the group's max / min magnitudes,
-// with the cap and the S-range guard; S = 2^(k log2 max - log2 448) rounded once.
+// k correctly rounded from double-float logs of the group's max / min
+// magnitudes (Lmx, Lmn: log2 of mx, mn), with the cap and the S-range guard;
+// S = 2^(k log2 max - log2 448) rounded once.
+__device__ __forceinline__ void k_and_S_logs(float mx, float mn, F2 Lmx, F2 Lmn,
+                                             const df::Tables& t, float& k, float& S) {
+    if (!(mx > 0.0f)) {
+        k = 1.0f;
+        S = 0.0f;
+        return;
+    }
+    bool slow = false;
+    k = df::k_certain(mx, mn, Lmx, Lmn, k_consts(), slow);
+    if (slow) atomicAdd(&g_recompute[1], 1ull);
+    S = df::exp2_df(df::add2(df::mul21(Lmx, k), df::neg2(const_df(kLog2_448Df))), t);
+}
+
+// The same with the logs formed here.
 __device__ __forceinline__ void k_and_S(float mx, float mn, const df::Tables& t, float& k,
                                         float& S) {
     if (!(mx > 0.0f)) {
@@ -230,34 +255,8 @@ __device__ __forceinline__ void k_and_S(float mx, float mn, const df::Tables& t,
         return;
     }
     const F2 Lmx = df::log2_df(mx, t);
-    k = 1.0f;
-    if (mn > 0.0f && mn < mx) {
-        const F2 Lmn = df::log2_df(mn, t);
-        k = fminf(df::div22_rn(const_df(kLog2RDf), df::add2(Lmx, df::neg2(Lmn))), kKCap);
-    }
-    if (Lmx.hi < 0.0f)
-        k = fminf(k, df::div22_rn(const_df(kGuardLoDf), Lmx));
-    else if (Lmx.hi > 0.0f)
-        k = fminf(k, df::div22_rn(const_df(kGuardHiDf), Lmx));
-    S = df::exp2_df(df::add2(df::mul21(Lmx, k), df::neg2(const_df(kLog2_448Df))), t);
-}
-
-// The same from logs computed elsewhere (Lmx, Lmn: log2 of mx, mn).
-__device__ __forceinline__ void k_and_S_logs(float mx, float mn, F2 Lmx, F2 Lmn,
-                                             const df::Tables& t, float& k, float& S) {
-    if (!(mx > 0.0f)) {
-        k = 1.0f;
-        S = 0.0f;
-        return;
-    }
-    k = 1.0f;
-    if (mn > 0.0f && mn < mx)
-        k = fminf(df::div22_rn(const_df(kLog2RDf), df::add2(Lmx, df::neg2(Lmn))), kKCap);
-    if (Lmx.hi < 0.0f)
-        k = fminf(k, df::div22_rn(const_df(kGuardLoDf), Lmx));
-    else if (Lmx.hi > 0.0f)
-        k = fminf(k, df::div22_rn(const_df(kGuardHiDf), Lmx));
-    S = df::exp2_df(df::add2(df::mul21(Lmx, k), df::neg2(const_df(kLog2_448Df))), t);
+    const F2 Lmn = (mn > 0.0f && mn < mx) ? df::log2_df(mn, t) : Lmx;
+    k_and_S_logs(mx, mn, Lmx, Lmn, t, k, S);
 }
 
 // Encoding constants: r = |x| * inv, y = 2^(k log2 r + cz).  A subnormal max
@@ -398,6 +397,7 @@ struct GroupRec {
     F2 rkd[2];           // 1/k
     float P[2];          // fast-path factor
     float S[2];          // stored S
+    float kst[2];        // stored k
     float eps[2];        // fast-path error bound
     float fmx[2];        // fast max |m|, max v
     float fmn[2];        // fast smallest non-zero
@@ -480,6 +480,7 @@ step_kernel_cta(const StepArgs a) {
         r.rkd[sm_] = p.rkd;
         r.P[sm_] = p.P;
         r.S[sm_] = S;
+        r.kst[sm_] = k;
         r.eps[sm_] = fast_err(p.rkd.hi);
     }
     __syncthreads();
@@ -604,7 +605,7 @@ step_kernel_cta(const StepArgs a) {
                                       r.fmn[1], r.gmx);
         const CandTest ct = cand_test(win, s, a.omb1);
         const F2 A = r.A[sm_], rkd = r.rkd[sm_];
-        const float S = r.S[sm_];
+        const float S = r.S[sm_], kst = r.kst[sm_];
         const float beta = second ? a.beta2 : a.beta1, omb = second ? a.omb2 : a.omb1;
         float best = is_max ? 0.0f : kInf;
         uint32_t h = r.holders[s];
@@ -690,7 +691,7 @@ step_kernel_cta(const StepArgs a) {
                 const int e = __ffs(msk) - 1;
                 msk &= msk - 1u;
                 const float x = exact_moment(byte_of(cw, e), bf16_of(gw, e), second, A, rkd, S,
-                                             beta, omb, tab, lg_hi, lg_lo);
+                                             kst, beta, omb, tab, lg_hi, lg_lo);
                 vals[chunk_slot(th, e >> 2) + (e & 3)] = x;   // encoded from the exact value
                 const float ax = fabsf(x);
                 if (is_max) best = fmaxf(best, ax);
@@ -812,15 +813,15 @@ step_kernel_thread(const StepArgs a) {
             const bool cv = cand(v[e], fabsf(gf), cvq, cand_test(win, 2, a.omb1)) ||
                             cand(v[e], fabsf(gf), cvq, cand_test(win, 3, a.omb1));
             if (cm) {
-                m[e] = exact_moment(byte_of(c.mq, e), gf, false, pm.A, pm.rkd, pm.S, a.beta1,
-                                    a.omb1, tab, lg_hi, lg_lo);
+                m[e] = exact_moment(byte_of(c.mq, e), gf, false, pm.A, pm.rkd, pm.S, md.y,
+                                    a.beta1, a.omb1, tab, lg_hi, lg_lo);
                 const float ax = fabsf(m[e]);
                 ex[0] = fmaxf(ex[0], ax);
                 if (ax > 0.0f) ex[1] = fminf(ex[1], ax);
             }
             if (cv) {
-                v[e] = exact_moment(byte_of(c.vq, e), gf, true, pv.A, pv.rkd, pv.S, a.beta2,
-                                    a.omb2, tab, lg_hi, lg_lo);
+                v[e] = exact_moment(byte_of(c.vq, e), gf, true, pv.A, pv.rkd, pv.S, md.w,
+                                    a.beta2, a.omb2, tab, lg_hi, lg_lo);
                 const float ax = fabsf(v[e]);
                 ex[2] = fmaxf(ex[2], ax);
                 if (ax > 0.0f) ex[3] = fminf(ex[3], ax);
@@ -884,6 +885,15 @@ cudaError_t launch_step(const StepArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t read_recompute_counts(unsigned long long out[2], bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_recompute, sizeof(unsigned long long) * 2);
+    if (e == cudaSuccess && reset) {
+        const unsigned long long zero[2] = {0ull, 0ull};
+        e = cudaMemcpyToSymbol(g_recompute, zero, sizeof(zero));
+    }
+    return e;
+}
 
 cudaError_t launch_adamw_dre_step(const StepArgs& a, int G, cudaStream_t stream) {
     switch (G) {

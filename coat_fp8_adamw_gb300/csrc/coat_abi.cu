@@ -182,6 +182,16 @@ coat_status coat_dre_dequantize(const uint8_t* q, const float* scale, const floa
     return from_cuda(coat::launch_dre_dequantize(a, G, static_cast<cudaStream_t>(stream)));
 }
 
+coat_status coat_exact_recompute_counts(uint64_t counts[2], int32_t reset) {
+    if (!counts) return COAT_ERR_INVALID_ARG;
+    unsigned long long c[2] = {0ull, 0ull};
+    const cudaError_t e = coat::read_recompute_counts(c, reset != 0);
+    if (e != cudaSuccess) return COAT_ERR_CUDA;
+    counts[0] = c[0];
+    counts[1] = c[1];
+    return COAT_OK;
+}
+
 const char* coat_status_string(coat_status s) {
     switch (s) {
         case COAT_OK: return "ok";
@@ -197,6 +207,6 @@ const char* coat_status_string(coat_status s) {
 
 double coat_r_e4m3(void) { return 448.0 * 512.0; }
 
-int32_t coat_version(void) { return 101; }
+int32_t coat_version(void) { return 200; }
 
 }  // extern "C"

@@ -17,6 +17,7 @@
 #define COAT_CONST __constant__
 #include "coat_tables.inc"
 #include "coat_df.cuh"
+#include "coat_round.cuh"
 
 namespace coat {
 
@@ -26,7 +27,6 @@ constexpr int kThreads = 256;    // threads per CTA
 // log2(448), log2(R_E4M3) = log2(448 * 2^9), the k cap, and the S-range guard
 // numerators (log2 448 - 125, log2 448 + 126), as float constants.
 constexpr float kLog2_448 = 8.8073549220576041f;
-constexpr float kLog2_448_minus9 = -0.19264507794239588f;  // log2(448) - 9
 constexpr float kLog2R = 17.807354922057604f;
 constexpr float kKCap = 8.0f;
 constexpr float kGuardLo = 8.8073549220576041f - 125.0f;
@@ -89,61 +89,6 @@ __device__ __forceinline__ uint4 ld_cs(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_cs(float4* p, float4 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_cs(uint4* p, uint4 v) { __stcs(p, v); }
 
-// ---------------------------------------------------------------------------
-// x > 0 finite (normal or subnormal): x = 2^e * u with u in [1, 2).
-// Returns e as an exactly representable float and log2(u) in [0, 1).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void split_log2(float x, float& e, float& log2u) {
-    uint32_t b = __float_as_uint(x);
-    int ex = (int)((b >> 23) & 0xFFu);
-    if (ex == 0) {  // subnormal: scale by 2^24 (exact)
-        b = __float_as_uint(x * 16777216.0f);
-        ex = (int)((b >> 23) & 0xFFu) - 24;
-    }
-    const float u = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
-    e = (float)(ex - 127);
-    log2u = log2f(u);
-}
-
-// 2^(hi + lo) for |lo| small, hi any finite value, with the integer part of hi
-// applied exactly.
-__device__ __forceinline__ float exp2_split(float hi, float lo) {
-    const float n = rintf(hi);
-    float f = (hi - n) + lo;           // hi - n is exact
-    const float n2 = rintf(f);
-    f -= n2;
-    return ldexpf(exp2f(f), (int)(n + n2));
-}
-
-// Parameters that turn a stored (S, k) into dequantized values:
-//   x = sign(q) * P * 2^(L(q) / k),  P = (448 S)^(1/k),  L(q) = log2(|E4M3(q)|/448)
-struct DequantParams {
-    float P;   // (448 S)^(1/k): the magnitude code 0x7E dequantizes to exactly P
-    float rk;  // 1/k
-};
-
-__device__ __forceinline__ DequantParams dequant_params(float S, float k) {
-    DequantParams d;
-    const float rk = __frcp_rn(k);
-    d.rk = rk;
-    if (!(S > 0.0f)) {
-        d.P = 0.0f;
-        return d;
-    }
-    // log2(448 S) = (e + 9) + (log2 u + log2(448) - 9)   [integer + small]
-    float e, l;
-    split_log2(S, e, l);
-    const float nhi = e + 9.0f;                    // exact integer
-    const float nlo = l + kLog2_448_minus9;        // in [-0.2, 0.81)
-    const float rk_lo = __fmul_rn(fmaf(-k, rk, 1.0f), rk);  // 1/k = rk + rk_lo
-    // t = (nhi + nlo) * (rk + rk_lo)
-    const float p = __fmul_rn(nhi, rk);
-    const float pe = fmaf(nhi, rk, -p);            // exact product error
-    const float tlo = fmaf(nlo, rk, fmaf(nhi, rk_lo, pe));
-    d.P = exp2_split(p, tlo);
-    return d;
-}
-
 // Fresh per-group parameters from the group's max and smallest non-zero
 // magnitude (section 3: R_X = max/min, k = log_{R_X} R_E4M3, S = max|f(X)|/448
 // = max^k / 448), with the library's cap and S-range guard.
@@ -179,9 +124,16 @@ __device__ __forceinline__ df::F2 const_df(const unsigned int* p) {
     return df::F2{__uint_as_float(p[0]), __uint_as_float(p[1])};
 }
 
-// Fresh per-group parameters with k rounded once to fp32 from a ~2^-44
-// accurate value (so it equals the correctly rounded k except within 2^-44
-// of a rounding tie) and S = 2^(k log2 max - log2 448) rounded once.
+// The exponent rule's constants (R_E4M3 = 448 / 2^-9, cap 8, S kept in
+// [2^-125, 2^126]) for df::k_certain.
+__device__ __forceinline__ df::KConsts k_consts() {
+    return df::KConsts{const_df(kLog2RDf), const_df(kGuardLoDf), const_df(kGuardHiDf), kKCap,
+                       448.0 * 512.0, -125.0, 126.0};
+}
+
+// Fresh per-group parameters with k correctly rounded to fp32 (double-float
+// logs and quotient, rounded once when that is certain, float64 otherwise)
+// and S = 2^(k log2 max - log2 448) rounded once.
 __device__ __forceinline__ QuantParams quant_params_precise(float mx, float mn,
                                                             const df::Tables& t) {
     QuantParams q;
@@ -192,29 +144,14 @@ __device__ __forceinline__ QuantParams quant_params_precise(float mx, float mn,
         return q;
     }
     const df::F2 Lmx = df::log2_df(mx, t);
-    float k = 1.0f;
-    if (mn < mx) {
-        const df::F2 Lmn = df::log2_df(mn, t);
-        const df::F2 D = df::add2(Lmx, df::neg2(Lmn));
-        k = fminf(df::div22_rn(const_df(kLog2RDf), D), kKCap);
-    }
-    if (Lmx.hi < 0.0f)
-        k = fminf(k, df::div22_rn(const_df(kGuardLoDf), Lmx));
-    else if (Lmx.hi > 0.0f)
-        k = fminf(k, df::div22_rn(const_df(kGuardHiDf), Lmx));
+    const df::F2 Lmn = (mn > 0.0f && mn < mx) ? df::log2_df(mn, t) : Lmx;
+    bool slow = false;
+    const float k = df::k_certain(mx, mn, Lmx, Lmn, k_consts(), slow);
     const df::F2 e = df::add2(df::mul21(Lmx, k), df::neg2(const_df(kLog2_448Df)));
     q.k = k;
     q.S = df::exp2_df(e, t);
     q.inv_mx = __frcp_rn(mx);
     return q;
-}
-
-// Dequantize one code: sign(q) * P * 2^(L(q) * rk).
-__device__ __forceinline__ float dequant_one(const float* s_log_tab, uint32_t code, float P,
-                                             float rk) {
-    const float L = s_log_tab[code & 0x7Fu];
-    const float mag = __fmul_rn(P, ex2_approx(__fmul_rn(L, rk)));
-    return __uint_as_float(__float_as_uint(mag) | ((code & 0x80u) << 24));
 }
 
 // Scaled, expanded value y = 448 sign(x) (|x| / max)^k, ready for E4M3 rounding.

@@ -142,11 +142,16 @@ COAT_HD F2 div21(F2 a, float b) {
     const float r = add(fma(-q, b, a.hi), a.lo);  // a.hi - q b is exact for a rounded quotient
     return fast_two_sum(q, div(r, b));
 }
-// a / b for two double-floats, rounded once to the nearest float
-COAT_HD float div22_rn(F2 a, F2 b) {
+// a / b for two double-floats as an unrounded pair q + c (|c| <= ulp(q))
+COAT_HD F2 div22_parts(F2 a, F2 b) {
     const float q = div(a.hi, b.hi);
     const float r = sub(add(fma(-q, b.hi, a.hi), a.lo), mul(q, b.lo));
-    return add(q, div(r, b.hi));
+    return {q, div(r, b.hi)};
+}
+// a / b for two double-floats, rounded once to the nearest float
+COAT_HD float div22_rn(F2 a, F2 b) {
+    const F2 p = div22_parts(a, b);
+    return add(p.hi, p.lo);
 }
 
 // --- constants (double-float) ---
@@ -192,8 +197,9 @@ COAT_HD F2 log2_df(float x, const Tables& t) {
     return two_sum(whole.hi, add(whole.lo, frac.lo));
 }
 
-// 2^z for a double-float z, rounded once to float (normal results).
-COAT_HD float exp2_df(F2 z, const Tables& t) {
+// 2^z for a double-float z as 2^n (m.hi + m.lo), with m.hi + m.lo in about
+// [0.7, 1.42] not yet rounded: the caller rounds m once and scales it by 2^n.
+COAT_HD F2 exp2_df_parts(F2 z, const Tables& t, int& n_out) {
     const float n = rint(z.hi);
     const F2 f = two_sum(sub(z.hi, n), z.lo);      // |f| <= 0.5 + tiny
     const float jf = rint(mul(f.hi, 32.0f));       // -16..16 for a normalized z
@@ -218,8 +224,15 @@ COAT_HD float exp2_df(F2 z, const Tables& t) {
     const F2 p = two_prod(T.hi, em1.hi);
     const F2 h = two_sum(T.hi, p.hi);
     const float lo = add(add(h.lo, p.lo), fma(T.hi, em1.lo, fma(T.lo, em1.hi, T.lo)));
-    const float m = add(h.hi, lo);                  // rounded once
-    return scale2(m, (int)n);
+    n_out = (int)n;
+    return {h.hi, lo};
+}
+
+// 2^z for a double-float z, rounded once to float (normal results).
+COAT_HD float exp2_df(F2 z, const Tables& t) {
+    int n = 0;
+    const F2 m = exp2_df_parts(z, t, n);
+    return scale2(add(m.hi, m.lo), n);              // rounded once
 }
 
 // round-to-nearest of a*b + c*d for floats, via error-free products and sum

@@ -39,6 +39,8 @@ struct DequantArgs {
 };
 
 cudaError_t launch_adamw_dre_step(const StepArgs& a, int G, cudaStream_t stream);
+// the step kernel's float64-recomputation counters on the current device
+cudaError_t read_recompute_counts(unsigned long long out[2], bool reset);
 
 }  // namespace coat
 

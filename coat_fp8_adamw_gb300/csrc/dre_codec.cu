@@ -143,25 +143,78 @@ dre_quantize_kernel(const QuantArgs a) {
     }
 }
 
+// Per-group parameters of the dequantizer: 2^z with z = log2(448 S) / k split
+// as Pm 2^Pe, Pm = 2^(z - Pe) rounded once (in about [0.7, 1.42]) and Pe the
+// integer nearest z, formed in double-float; 1/k as a double-float.  An
+// all-zero group (S = 0) gets Pm = 0.
+struct DequantGroup {
+    float Pm;
+    int Pe;
+    float rk_hi, rk_lo;
+};
+
+__device__ __forceinline__ DequantGroup dequant_group(float S, float k, const df::Tables& t) {
+    DequantGroup d;
+    const df::F2 rkd = df::div21(df::F2{1.0f, 0.0f}, k);
+    d.rk_hi = rkd.hi;
+    d.rk_lo = rkd.lo;
+    if (!(S > 0.0f)) {
+        d.Pm = 0.0f;
+        d.Pe = 0;
+        return d;
+    }
+    const df::F2 z = df::mul22(df::add2(df::log2_df(S, t), const_df(kLog2_448Df)), rkd);
+    const float n0 = rintf(z.hi);
+    d.Pm = df::exp2_df(df::F2{__fsub_rn(z.hi, n0), z.lo}, t);
+    d.Pe = (int)n0;
+    return d;
+}
+
+// One code: sign(q) (|E4M3(q)| S)^(1/k) = sign(q) Pm 2^Pe 2^(L / k) with
+// L = log2(|E4M3(q)| / 448) from the double-float table.  L / k is formed as
+// a double-float product, its integer part n is applied exactly and only the
+// fraction f (|f| <= 1/2) goes through the SFU exp2 (relative error <= 2^-22
+// there), so the result is within about 2^-22 + 2^-23 of the exact value.  A
+// result outside the normal fp32 range is scaled with one more rounding.
+__device__ __forceinline__ float dequant_code(const float2* s_L, uint32_t code, const DequantGroup& d) {
+    const uint32_t mag = code & 0x7Fu;
+    if (mag == 0u || !(d.Pm > 0.0f)) return 0.0f;
+    const float2 L = s_L[mag];
+    const float p = __fmul_rn(L.x, d.rk_hi);
+    const float t = fmaf(L.x, d.rk_lo, fmaf(L.y, d.rk_hi, fmaf(L.x, d.rk_hi, -p)));
+    const float n = rintf(p);
+    const float f = __fadd_rn(__fsub_rn(p, n), t);
+    const float y = __fmul_rn(d.Pm, ex2_ftz(f));
+    const int ni = (int)n + d.Pe;
+    const uint32_t yb = __float_as_uint(y);
+    const int eb = (int)((yb >> 23) & 0xFFu) + ni;
+    const float x = (eb >= 1 && eb <= 254) ? __uint_as_float(yb + ((uint32_t)ni << 23))
+                                           : df::scale2(y, ni);
+    return __uint_as_float(__float_as_uint(x) | ((code & 0x80u) << 24));
+}
+
 template <int G>
 __global__ void __launch_bounds__(kThreads)
 dre_dequantize_kernel(const DequantArgs a) {
     using Gm = Geom<G>;
-    __shared__ float s_log[128];
-    __shared__ float s_P[Gm::kGpc], s_rk[Gm::kGpc];
-    for (int i = threadIdx.x; i < 128; i += kThreads) s_log[i] = __uint_as_float(kLog2Frac448Hi[i]);
+    __shared__ float2 s_L[128];
+    __shared__ SmemTables st;
+    __shared__ DequantGroup s_d[Gm::kGpc];
+    for (int i = threadIdx.x; i < 128; i += kThreads)
+        s_L[i] = make_float2(__uint_as_float(kLog2Frac448Hi[i]), __uint_as_float(kLog2Frac448Lo[i]));
+    load_smem_tables(st, threadIdx.x, kThreads);
+    __syncthreads();
+    const df::Tables tab = tables_of(st);
     if constexpr (Gm::kJobs) {
         // one thread per group of the CTA forms its dequantization parameters
         const int64_t gcta = (int64_t)blockIdx.x * Gm::kGpc;
         for (int j = threadIdx.x; j < Gm::kGpc; j += kThreads) {
             float S = 0.0f, k = 1.0f;
             if ((gcta + j) * G < a.n) { S = a.scale[gcta + j]; k = a.k[gcta + j]; }
-            const DequantParams d = dequant_params(S, k);
-            s_P[j] = d.P;
-            s_rk[j] = d.rk;
+            s_d[j] = dequant_group(S, k, tab);
         }
+        __syncthreads();
     }
-    __syncthreads();
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t base = tid * kVec;
     if (base >= a.n) return;
@@ -178,25 +231,21 @@ dre_dequantize_kernel(const DequantArgs a) {
             if (base + e < a.n) q[e / 4] |= (uint32_t)a.q[base + e] << (8 * (e & 3));
     }
     const int64_t g0 = base / G;
-    DequantParams d[Gm::kGroups];
+    DequantGroup d[Gm::kGroups];
     if constexpr (Gm::kJobs) {
-        const int gl = (int)((threadIdx.x * kVec) / G);
-        d[0].P = s_P[gl];
-        d[0].rk = s_rk[gl];
+        d[0] = s_d[(threadIdx.x * kVec) / G];
     } else {
 #pragma unroll
         for (int j = 0; j < Gm::kGroups; ++j) {
             float S = 0.0f, k = 1.0f;
             if ((g0 + j) * G < a.n) { S = a.scale[g0 + j]; k = a.k[g0 + j]; }
-            d[j] = dequant_params(S, k);
+            d[j] = dequant_group(S, k, tab);
         }
     }
     float x[kVec];
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) {
-        const int j = e / Gm::kElems;
-        x[e] = dequant_one(s_log, (q[e / 4] >> (8 * (e & 3))) & 0xFFu, d[j].P, d[j].rk);
-    }
+    for (int e = 0; e < kVec; ++e)
+        x[e] = dequant_code(s_L, (q[e / 4] >> (8 * (e & 3))) & 0xFFu, d[e / Gm::kElems]);
     if (full) {
         float4* xp = reinterpret_cast<float4*>(a.x + base);
 #pragma unroll

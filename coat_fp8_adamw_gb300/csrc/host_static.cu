@@ -10,9 +10,7 @@
 // file-scope __device__ array of this translation unit instead: the CUDA
 // runtime reserves it on a device when it loads this file's module there, and
 // the call itself allocates nothing.
-#include <atomic>
 #include <cstdint>
-#include <mutex>
 #include <cuda_runtime.h>
 
 #include "coat.h"
@@ -21,15 +19,10 @@
 namespace {
 
 constexpr int64_t kChunkQuantum = 4096;  // chunk sizes are multiples of this (and of G)
-constexpr int kMaxDevices = 64;
 
 // The scratch of one chunk; nothing in it has to start at zero (every byte the
 // kernel reads is copied in by the same call first).
 __device__ __align__(256) unsigned char g_static_scratch[COAT_STATIC_SCRATCH_BYTES];
-
-// Its device address on each device, resolved once per device.
-std::atomic<void*> g_scratch_ptr[kMaxDevices];
-std::mutex g_setup_mutex;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -48,25 +41,29 @@ bool is_host(const void* p) {
     return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
 }
 
-// The scratch's address on the current device.  The first call on a device
-// looks it up with cudaGetSymbolAddress, which may load this module there.
+// The scratch's address on the current device (the array's name is only a
+// host-side stand-in).  It is looked up on every call: a lookup allocates
+// nothing, and a cached address would outlive a device reset, after which the
+// module is loaded again and the array may sit elsewhere.  The first lookup
+// on a device may load this module there.
 cudaError_t scratch_on_current_device(unsigned char** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
-    if (!p) {
-        std::lock_guard<std::mutex> lock(g_setup_mutex);
-        p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
-        if (!p) {
-            e = cudaGetSymbolAddress(&p, g_static_scratch);
-            if (e != cudaSuccess) return e;
-            g_scratch_ptr[dev].store(p, std::memory_order_release);
-        }
-    }
     *out = static_cast<unsigned char*>(p);
     return cudaSuccess;
+}
+
+// A stream that belongs to another device than the current one would queue
+// the copies before the launch fails: refuse it first.
+bool stream_on_current_device(cudaStream_t s) {
+    if (s == nullptr) return true;   // the legacy default stream of the current device
+    int cur = -1, dev = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(s, &dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return cur == dev;
 }
 
 }  // namespace
@@ -99,6 +96,7 @@ coat_status coat_fp8_adamw_step_host_static(float* w, const uint16_t* g, uint8_t
     coat::StepArgs proto;
     st = coat::make_step_args(beta1, beta2, lr, eps, weight_decay, step, proto);
     if (st != COAT_OK) return st;
+    if (!stream_on_current_device(static_cast<cudaStream_t>(stream))) return COAT_ERR_INVALID_ARG;
     unsigned char* scratch = nullptr;
     cudaError_t err = scratch_on_current_device(&scratch);
     if (err != cudaSuccess) return COAT_ERR_CUDA;

@@ -37,7 +37,7 @@
  *     are host pointers.  The library allocates no memory and keeps no state
  *     between calls (coat_fp8_adamw_step_host creates and destroys its three
  *     streams and one event within the call; coat_fp8_adamw_step_host_static
- *     keeps its scratch's device address per device).
+ *     uses a fixed device array of the library as its scratch).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call is asynchronous on that stream, except
  *     coat_fp8_adamw_step_host and coat_fp8_adamw_step_host_static, which
@@ -164,11 +164,14 @@ size_t coat_fp8_adamw_step_host_workspace_bytes(int64_t chunk_params, int32_t G)
  *                 0 = the largest chunk that fits the scratch (about 2.06
  *                 million parameters at G = 128, about 0.7 million at G = 1).
  *
- * Set-up: the first call on a device, made with that device current, looks
- * up the scratch's device address (cudaGetSymbolAddress), which may load the
- * module on that device; make that first call before any stream capture
- * begins.  Nothing in the scratch has to start at zero: each chunk's bytes
- * are copied in by the same call before the kernel reads them.
+ * Set-up: every call looks up the scratch's device address on the current
+ * device (cudaGetSymbolAddress, which allocates nothing; the address is not
+ * cached, so a device reset between calls is safe).  The first call on a
+ * device may load the library's module there: make that first call before
+ * any stream capture begins.  `stream` must belong to the current device
+ * (COAT_ERR_INVALID_ARG otherwise, before anything is copied).  Nothing in
+ * the scratch has to start at zero: each chunk's bytes are copied in by the
+ * same call before the kernel reads them.
  * One scratch per device: calls that overlap in time on one device (from
  * several host threads, or on several streams) race on it; the caller must
  * serialize them.
@@ -233,6 +236,24 @@ coat_status coat_act_quantize_fp8(const uint16_t *x, int64_t M, int64_t N, int32
  */
 coat_status coat_dre_dequantize(const uint8_t *q, const float *scale, const float *k, int64_t n,
                                 int32_t G, float *x, void *stream);
+
+/*
+ * Diagnostics of the step's correctly rounded exact path.  The step
+ * re-evaluates every group's extreme moments and its exponent k in
+ * double-float arithmetic and rounds each once to float32 (COAT review page,
+ * section 3: the dequantized state is an fp32 tensor X_FP32, and k and S follow
+ * from the group's max|X| and min|X|).  When a double-float value lies too close
+ * to an fp32 rounding midpoint for that rounding to be certain, the value is
+ * recomputed in float64 from its definition.  This call reads how often that
+ * happened on the current device since the library was loaded there (or since
+ * the last reset):
+ *   counts[0]  dequantized moments recomputed,
+ *   counts[1]  exponents k recomputed.
+ * reset != 0 clears both counters after reading them.  The call synchronizes
+ * with the current device (it copies from device memory) and must not overlap
+ * a running step if exact counts are wanted.
+ */
+coat_status coat_exact_recompute_counts(uint64_t counts[2], int32_t reset);
 
 /* Static description of a status code (never NULL). */
 const char *coat_status_string(coat_status status);

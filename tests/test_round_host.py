@@ -5,6 +5,7 @@ import os
 import shutil
 import subprocess
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -89,3 +90,92 @@ def test_float64_recomputations_match_the_oracle(tmp_path):
             continue
         g = oracle.dre_group(np.array([mx, mn], np.float32))
         assert np.float32(L.kk(float(mx), float(mn))) == np.float32(g["k"]), (float(mx), float(mn))
+
+
+def _near_midpoint_dequant_cases(rng, N):
+    dec = oracle_mod().e4m3_decode_all()
+    finite = np.array([c for c in range(1, 127) if c != 0x7F], dtype=np.uint8)
+    codes = rng.choice(finite, N)
+    S = np.exp2(rng.uniform(-110.0, 0.0, N)).astype(np.float32)
+    k = rng.uniform(0.6, 8.0, N).astype(np.float32)
+    x = (np.abs(dec[codes]) * S.astype(np.float64)) ** (1.0 / k.astype(np.float64))
+    ok = (x > 2.0 ** -126) & (x < 2.0 ** 127)
+    frac = x / np.spacing(x.astype(np.float32)).astype(np.float64)
+    dist = np.abs(frac - np.floor(frac) - 0.5)
+    return codes, S, k, ok, dist
+
+
+def oracle_mod():
+    import oracle
+    return oracle
+
+
+def test_exact_path_dequant_matches_the_oracle_at_hard_roundings(tmp_path):
+    """The step kernel's exact dequantization (host build of the same code)
+    equals the oracle's correctly rounded fp32 value bit for bit, for values
+    within 1e-5 ulp of an fp32 midpoint (decided by the float64 path), between
+    1e-5 and 1e-3 ulp, and at random; the float64 path stays rare at random."""
+    import _exact_path
+    oracle = oracle_mod()
+    exe = _exact_path.build(tmp_path)
+    rng = np.random.default_rng(41)
+    codes, S, k, ok, dist = _near_midpoint_dequant_cases(rng, 3_000_000)
+    hard = np.nonzero(ok & (dist < 1e-5))[0][:80]
+    medium = np.nonzero(ok & (dist >= 1e-5) & (dist < 1e-3))[0][:300]
+    rand = np.nonzero(ok)[0][:20000]
+    assert hard.size >= 30
+    for name, idx in (("hard", hard), ("medium", medium), ("random", rand)):
+        got, slow = _exact_path.dequant(exe, codes[idx], S[idx], k[idx])
+        want = np.array([oracle.dre_dequantize(codes[i:i + 1], S[i:i + 1], k[i:i + 1], 1)[0]
+                         for i in idx], np.float32)
+        bad = np.nonzero(got.view(np.uint32) != np.abs(want).view(np.uint32))[0]
+        assert bad.size == 0, (name, [(int(codes[idx[j]]), float(S[idx[j]]), float(k[idx[j]]))
+                                      for j in bad[:5]])
+        print(name, idx.size, "float64 path", int(slow.sum()))
+        if name == "hard":
+            assert slow.mean() > 0.5            # the band of doubt covers these
+        if name == "random":
+            assert slow.mean() < 1e-3
+
+
+def test_exact_path_k_matches_the_oracle_at_hard_roundings(tmp_path):
+    """The step kernel's k (host build of the same code) equals the oracle's
+    bit for bit for k within 1e-5 ulp of an fp32 midpoint, at random, and where
+    the cap or the S-range guard decides."""
+    import _exact_path
+    oracle = oracle_mod()
+    exe = _exact_path.build(tmp_path)
+    rng = np.random.default_rng(42)
+    N = 3_000_000
+    mx = np.exp2(rng.uniform(-40.0, 10.0, N)).astype(np.float32)
+    mn = (mx.astype(np.float64) * np.exp2(-rng.uniform(2.3, 40.0, N))).astype(np.float32)
+    kk = np.log(229376.0) / np.log(mx.astype(np.float64) / mn.astype(np.float64))
+    frac = kk / np.spacing(kk.astype(np.float32)).astype(np.float64)
+    dist = np.abs(frac - np.floor(frac) - 0.5)
+    free = kk < 7.9
+    hard = np.nonzero(free & (dist < 1e-5))[0][:60]
+    rand = np.arange(3000)
+    # guard-active (tiny or huge max) and cap-active (ratio below 4.68) pairs
+    lmx = rng.uniform(-140.0, 120.0, 3000)
+    ratio = np.where(rng.random(3000) < 0.3, rng.uniform(0.0, 2.3, 3000), rng.uniform(2.3, 40.0, 3000))
+    emx = np.exp2(lmx).astype(np.float32)
+    emn = np.exp2(lmx - ratio).astype(np.float32)
+    keep = (emn > 0) & np.isfinite(emx) & (emx > 0)
+    assert hard.size >= 30
+    cases = [("hard", mx[hard], mn[hard]), ("random", mx[rand], mn[rand]),
+             ("edges", emx[keep], emn[keep])]
+    for name, a, b in cases:
+        got, slow = _exact_path.kexp(exe, a, b)
+        want = np.array([oracle.dre_group(np.array([x, y], np.float32))["k"] for x, y in zip(a, b)],
+                        np.float32)
+        bad = np.nonzero(got != want)[0]
+        assert bad.size == 0, (name, [(float(a[j]), float(b[j]), float(got[j]), float(want[j]))
+                                      for j in bad[:5]])
+        print(name, a.size, "float64 path", int(slow.sum()))
+        if name == "hard":
+            # k's band of doubt is about 2^-43 (2 + |log2 max| + |log2 min|) /
+            # log2 R_X relative: a good part of values within 1e-5 ulp of a
+            # midpoint (6e-13 relative at most) lies inside it
+            assert slow.mean() > 0.25
+        if name == "random":
+            assert slow.mean() < 2e-3
