@@ -88,6 +88,14 @@ coat_status make_step_args(float beta1, float beta2, float lr, float eps, float 
     a.c2 = (float)(1.0 / bc2);
     a.eps = eps;
     a.decay = (float)(1.0 - (double)lr * (double)weight_decay);
+    const double c1 = (double)lr / bc1;
+    if (c1 > 0.0) {
+        a.sq = (float)(-std::sqrt(1.0 / bc2) / c1);
+        a.ep = (float)(-(double)eps / c1);
+    } else {
+        a.sq = 1.0f;
+        a.ep = INFINITY;
+    }
     return COAT_OK;
 }
 

@@ -20,6 +20,11 @@ struct StepArgs {
     float c2;          // 1 / (1 - beta2^t)
     float eps;
     float decay;       // 1 - lr * weight_decay
+    // the update's denominator scaled by -1/c1: -(sqrt(v c2) + eps) / c1 =
+    // sqrt(v) sq + ep, so that w - c1 m / (sqrt(v c2) + eps) = w + m / (sqrt(v) sq + ep)
+    // (lr = 0: sq = 1, ep = +inf, and the update term is 0)
+    float sq;          // -sqrt(c2) / c1
+    float ep;          // -eps / c1
 };
 
 struct QuantArgs {

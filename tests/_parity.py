@@ -45,7 +45,10 @@ def compare_w(gpu: np.ndarray, ref: np.ndarray, what: str = "w") -> dict:
     r = ref.astype(np.float64)
     err = np.abs(g - r)
     ok = err <= W_RTOL * np.abs(r) + W_ATOL
-    assert ok.all(), f"{what}: {int((~ok).sum())} weights outside tolerance, max err {err.max():.3e}"
+    if not ok.all():
+        i = int(np.argmax(err / (W_RTOL * np.abs(r) + W_ATOL)))
+        raise AssertionError(f"{what}: {int((~ok).sum())} weights outside tolerance, max err "
+                             f"{err.max():.3e}; worst at {i}: gpu {g[i]!r} ref {r[i]!r}")
     return {"w_max_rel": float((err / np.maximum(np.abs(r), 1e-30)).max())}
 
 

@@ -46,7 +46,7 @@ def _searched_cases(count, seed):
     rng = np.random.default_rng(seed)
     N = 4_000_000
     codes = rng.choice(np.arange(1, 0x7E, dtype=np.uint8), N)
-    S = np.exp2(rng.uniform(-110.0, 0.0, N)).astype(np.float32)
+    S = np.exp2(rng.uniform(-60.0, -2.0, N)).astype(np.float32)
     k = rng.uniform(1.05, 8.0, N).astype(np.float32)
     x = (np.abs(dec[codes]) * S.astype(np.float64)) ** (1.0 / k.astype(np.float64))
     ok = (x > 2.0 ** -120) & (x < 2.0 ** 100)
@@ -59,16 +59,19 @@ def _searched_cases(count, seed):
 def _groups(cases, G):
     """State and gradient of one group per case: element 0 holds the hard
     code, cancelled by its gradient; the other elements hold the largest code
-    and a zero gradient (the group maximum)."""
+    and a zero gradient (the group maximum).  Every second moment is stored as
+    the largest code with k = 1 and S = P^2 / 448, P = (448 S_m)^(1/k_m) the
+    largest first moment, so that v ~ m^2 as on an AdamW trajectory."""
     b1 = np.float32(HP["beta1"])
     n = len(cases) * G
     mq = np.full(n, 0x7E, np.uint8)
-    vq = np.zeros(n, np.uint8)
+    vq = np.full(n, 0x7E, np.uint8)
     meta = np.zeros((len(cases), 4), np.float32)
     g = np.zeros(n, np.float32)
     for i, (code, S, k) in enumerate(cases):
         mq[i * G] = code
-        meta[i] = (S, k, 0.0, 1.0)
+        pm = (448.0 * float(S)) ** (1.0 / float(k))
+        meta[i] = (S, k, np.float32(pm * pm / 448.0), 1.0)
         prev = float(oracle.dre_dequantize(np.array([code], np.uint8), np.array([S]),
                                            np.array([k]), 1)[0])
         g[i * G] = -float(b1) * prev * 0.95 / (1.0 - float(b1))

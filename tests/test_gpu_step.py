@@ -90,6 +90,20 @@ def test_adamw_like_state_every_group_size(G):
     check(gpu, ref, f"random G={G}")
 
 
+@pytest.mark.parametrize("G", [16, 64, 128, 256])
+def test_many_tiles_per_cta_with_ragged_tail(G):
+    """Enough parameters that every persistent CTA of the step kernel runs
+    several tiles of its double-buffered pipeline (more than 2048 parameters
+    times three CTAs per SM times the SM count), with a ragged last tile."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = 2048 * 3 * sms * 3 + 2048 * 5 + 333
+    rng = np.random.default_rng(1000 + G)
+    w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    g = synth.f32_to_bf16_bits((rng.standard_normal(n) * 10.0 ** rng.uniform(-5, -2, n)).astype(np.float32))
+    mq, vq, meta = P.adamw_like_state(n, G, 200 + G, oracle)
+    check(gpu_step(w, g, mq, vq, meta, G, 9), oracle_step(w, g, mq, vq, meta, G, 9), f"tiles G={G}")
+
+
 @pytest.mark.parametrize("n", [1, 5, 16, 17, 127, 128, 129, 255, 4097])
 def test_small_and_ragged_sizes(n):
     G = 128
