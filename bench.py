@@ -49,10 +49,14 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
-    p.add_argument("--report", default=None, choices=["dre-mse", "act-quant"],
+    p.add_argument("--report", default=None, choices=["dre-mse", "act-quant", "g-sweep"],
                    help="dre-mse: quantization error with and without the expansion on "
                         "AdamW-like moments, and the codec kernels' bandwidth; act-quant: "
-                        "bandwidth of the per-group FP8 activation quantizer (one GPU)")
+                        "bandwidth of the per-group FP8 activation quantizer (one GPU); "
+                        "g-sweep: the step over --sweep-workload for G in --sweep-G, one "
+                        "JSON line per G with its roofline and clocks")
+    p.add_argument("--sweep-workload", default="llama13b")
+    p.add_argument("--sweep-G", default="16,32,64,128,256")
     p.add_argument("--rows", type=int, default=32768, help="M of the act-quant report")
     p.add_argument("--cols", type=int, default=8192, help="N of the act-quant report")
     p.add_argument("--params", type=int, default=1 << 30,
@@ -164,8 +168,8 @@ def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "coat_fp8_adamw_gb300", "csrc")
     # every file the step kernel is compiled from (the C ABI header only declares)
-    for name in ("adamw_dre_step.cu", "coat_device.cuh", "coat_df.cuh", "coat_tables.inc",
-                 "coat_kernels.h"):
+    for name in ("adamw_dre_step.cu", "coat_device.cuh", "coat_df.cuh", "coat_round.cuh",
+                 "coat_tables.inc", "coat_kernels.h"):
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -427,10 +431,65 @@ def e2e_leg(args, coat, synth, torch, dev, w, g, mq, vq, meta, n, G, ng, hp, t):
     torch.cuda.profiler.stop()
     h2d = n * (4 + 2 + 1 + 1) + ng * 16
     d2h = n * (4 + 1 + 1) + ng * 16
+    link = link_bandwidth(torch, dev, hw, ws)
+    # the step's time if the copies ran at the measured link rates and the
+    # kernel were free: whichever of one direction alone and both together binds
+    bound_s = max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9),
+                  (h2d + d2h) / (link["bidir_gbs"] * 1e9))
+    per_step = el / args.e2e_steps
     return {"value": n * args.e2e_steps / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "chunk_params": chunk,
+            "link_gbs": link, "link_bound_params_per_s": n / bound_s,
+            "e2e_frac_of_link": bound_s / per_step,
             "note": "coat_fp8_adamw_step_host on pinned host buffers (state offloaded to host "
-                    "memory), host wall clock per call"}
+                    "memory), host wall clock per call; link_gbs: plain pinned copies measured "
+                    "in the same process just after (one direction, then both at once)"}
+
+
+def link_bandwidth(torch, dev, host_pinned, dev_buf, reps=4):
+    """Raw host<->device copy rates between pinned host memory and the device:
+    host->device, device->host, and both at once on two streams (each direction
+    its own buffers).  Timed with CUDA events on the copying streams."""
+    nb = min(dev_buf.numel() // 2, host_pinned.numel() * host_pinned.element_size() // 2, 1 << 30)
+    hb = host_pinned.view(torch.uint8)[: 2 * nb]
+    h_in, h_out = hb[:nb], hb[nb: 2 * nb]
+    d_in, d_out = dev_buf[:nb], dev_buf[nb: 2 * nb]
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn, streams):
+        for s in streams:
+            s.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in streams]
+        for (a, _), s in zip(evs, streams):
+            a.record(s)
+        fn()
+        for (_, b), s in zip(evs, streams):
+            b.record(s)
+        torch.cuda.synchronize()
+        return max(a.elapsed_time(b) for a, b in evs) / 1e3
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            for _ in range(reps):
+                d_in.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            for _ in range(reps):
+                h_out.copy_(d_out, non_blocking=True)
+
+    h2d()
+    d2h()
+    t_h2d = timed(h2d, [s1])
+    t_d2h = timed(d2h, [s2])
+
+    def both():
+        h2d()
+        d2h()
+    t_both = timed(both, [s1, s2])
+    return {"h2d_gbs": reps * nb / t_h2d / 1e9, "d2h_gbs": reps * nb / t_d2h / 1e9,
+            "bidir_gbs": 2 * reps * nb / t_both / 1e9, "bytes_per_copy": int(nb)}
 
 
 def report_dre_mse(args):
@@ -542,8 +601,83 @@ def report_act_quant(args):
     print(json.dumps(out), flush=True)
 
 
+def report_g_sweep(args):
+    """The step over one model-shaped parameter set for several group sizes
+    (the 13B configuration sweeps G = 16 ... 256): weights and three cycled
+    gradients are generated once, the state is reset for every G, and each G
+    gets warm-up steps, timed steps (CUDA events per launch on the launching
+    stream), clocks sampled while they run, and its roofline line."""
+    import torch
+
+    import coat_fp8_adamw_gb300 as coat
+    from coat_fp8_adamw_gb300 import synth
+    coat.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl0 = synth.workload(args.sweep_workload)
+    n = wl0.n
+    w = synth.init_weights_torch(wl0, dev)
+    grads = [synth.grad_torch(wl0, 1 + i, dev) for i in range(max(1, args.grads))]
+    hp = synth.HYPER
+    peak, peak_kind = measured_peak()
+    stream = torch.cuda.current_stream(dev)
+    for G in (int(x) for x in args.sweep_G.split(",")):
+        ng = coat.num_groups(n, G)
+        mq = torch.zeros(n, dtype=torch.uint8, device=dev)
+        vq = torch.zeros(n, dtype=torch.uint8, device=dev)
+        meta = torch.zeros(ng, 4, dtype=torch.float32, device=dev)
+        meta[:, 1] = 1.0
+        meta[:, 3] = 1.0
+        t = 0
+
+        def step():
+            nonlocal t
+            t += 1
+            coat.coat_fp8_adamw_step(w, grads[(t - 1) % len(grads)], mq, vq, meta, G, hp["beta1"],
+                                     hp["beta2"], hp["lr"], hp["eps"], hp["weight_decay"], t,
+                                     stream=stream)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        clocks = ClockSampler(0)
+        clocks.start()
+        time.sleep(0.3)
+        for a, b in evs:
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+        ms = [a.elapsed_time(b) for a, b in evs]
+        avg = statistics.mean(ms)
+        bpp = coat.bytes_per_param(G)
+        achieved = bpp * n / (avg / 1e3) / 1e9
+        print(json.dumps({"report": "g-sweep", "metric": METRIC, "value": n / (avg / 1e3),
+                          "unit": UNIT, "config": {"workload": f"{args.sweep_workload}-shaped "
+                                                   "parameter set", "G": G, "params": n,
+                                                   "groups": ng, "bytes_per_param": bpp,
+                                                   "gradients": f"{len(grads)} distinct seeded "
+                                                                "gradients, cycled"},
+                          "steps": args.steps, "warmup": args.warmup,
+                          "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
+                                       "unit": "GB/s", "frac": achieved / peak,
+                                       "peak_kind": f"{peak_kind} (copy bandwidth)",
+                                       "kernel": KERNEL, "avg_launch_ms": avg,
+                                       "median_launch_ms": statistics.median(ms),
+                                       "min_launch_ms": min(ms), "max_launch_ms": max(ms)},
+                          "clocks": clk}), flush=True)
+        del mq, vq, meta
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
+    if args.report == "g-sweep":
+        report_g_sweep(args)
+        return
     if args.report == "dre-mse":
         report_dre_mse(args)
         return

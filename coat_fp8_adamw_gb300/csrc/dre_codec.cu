@@ -193,13 +193,40 @@ __device__ __forceinline__ float dequant_code(const float2* s_L, uint32_t code, 
     return __uint_as_float(__float_as_uint(x) | ((code & 0x80u) << 24));
 }
 
+// Two 16-code chunks per thread (a CTA covers 2 x 4096 codes): the loads of
+// both are issued before any arithmetic, so twice the bytes are in flight
+// per thread (the per-code arithmetic is a dependent chain of ~15 operations).
+constexpr int kDqChunks = 2;
+
 template <int G>
 __global__ void __launch_bounds__(kThreads)
 dre_dequantize_kernel(const DequantArgs a) {
     using Gm = Geom<G>;
+    constexpr int kCtaCodes = kDqChunks * kThreads * kVec;
+    constexpr int kGpc = G >= 2 * kVec ? kCtaCodes / G : 1;   // groups per CTA (job form)
     __shared__ float2 s_L[128];
     __shared__ SmemTables st;
-    __shared__ DequantGroup s_d[Gm::kGpc];
+    __shared__ DequantGroup s_d[kGpc];
+    const int64_t cta0 = (int64_t)blockIdx.x * kCtaCodes;
+    // the codes first: their loads are in flight while the tables and groups are set up
+    uint32_t q[kDqChunks][kVec / 4];
+    int64_t base[kDqChunks];
+    bool full[kDqChunks];
+#pragma unroll
+    for (int c = 0; c < kDqChunks; ++c) {
+        base[c] = cta0 + (int64_t)(c * kThreads + threadIdx.x) * kVec;
+        full[c] = base[c] + kVec <= a.n;
+        if (full[c]) {
+            const uint4 t = ld_cs(reinterpret_cast<const uint4*>(a.q + base[c]));
+            q[c][0] = t.x; q[c][1] = t.y; q[c][2] = t.z; q[c][3] = t.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < kVec / 4; ++i) q[c][i] = 0u;
+#pragma unroll
+            for (int e = 0; e < kVec; ++e)
+                if (base[c] + e < a.n) q[c][e / 4] |= (uint32_t)a.q[base[c] + e] << (8 * (e & 3));
+        }
+    }
     for (int i = threadIdx.x; i < 128; i += kThreads)
         s_L[i] = make_float2(__uint_as_float(kLog2Frac448Hi[i]), __uint_as_float(kLog2Frac448Lo[i]));
     load_smem_tables(st, threadIdx.x, kThreads);
@@ -207,53 +234,43 @@ dre_dequantize_kernel(const DequantArgs a) {
     const df::Tables tab = tables_of(st);
     if constexpr (Gm::kJobs) {
         // one thread per group of the CTA forms its dequantization parameters
-        const int64_t gcta = (int64_t)blockIdx.x * Gm::kGpc;
-        for (int j = threadIdx.x; j < Gm::kGpc; j += kThreads) {
+        const int64_t gcta = cta0 / G;
+        for (int j = threadIdx.x; j < kGpc; j += kThreads) {
             float S = 0.0f, k = 1.0f;
             if ((gcta + j) * G < a.n) { S = a.scale[gcta + j]; k = a.k[gcta + j]; }
             s_d[j] = dequant_group(S, k, tab);
         }
         __syncthreads();
     }
-    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const int64_t base = tid * kVec;
-    if (base >= a.n) return;
-    const bool full = base + kVec <= a.n;
-    uint32_t q[kVec / 4];
-    if (full) {
-        const uint4 t = ld_cs(reinterpret_cast<const uint4*>(a.q + base));
-        q[0] = t.x; q[1] = t.y; q[2] = t.z; q[3] = t.w;
-    } else {
 #pragma unroll
-        for (int i = 0; i < kVec / 4; ++i) q[i] = 0u;
+    for (int c = 0; c < kDqChunks; ++c) {
+        if (base[c] >= a.n) continue;
+        const int64_t g0 = base[c] / G;
+        DequantGroup d[Gm::kGroups];
+        if constexpr (Gm::kJobs) {
+            d[0] = s_d[(int)(g0 - cta0 / G)];
+        } else {
 #pragma unroll
-        for (int e = 0; e < kVec; ++e)
-            if (base + e < a.n) q[e / 4] |= (uint32_t)a.q[base + e] << (8 * (e & 3));
-    }
-    const int64_t g0 = base / G;
-    DequantGroup d[Gm::kGroups];
-    if constexpr (Gm::kJobs) {
-        d[0] = s_d[(threadIdx.x * kVec) / G];
-    } else {
-#pragma unroll
-        for (int j = 0; j < Gm::kGroups; ++j) {
-            float S = 0.0f, k = 1.0f;
-            if ((g0 + j) * G < a.n) { S = a.scale[g0 + j]; k = a.k[g0 + j]; }
-            d[j] = dequant_group(S, k, tab);
+            for (int j = 0; j < Gm::kGroups; ++j) {
+                float S = 0.0f, k = 1.0f;
+                if ((g0 + j) * G < a.n) { S = a.scale[g0 + j]; k = a.k[g0 + j]; }
+                d[j] = dequant_group(S, k, tab);
+            }
         }
-    }
-    float x[kVec];
-#pragma unroll
-    for (int e = 0; e < kVec; ++e)
-        x[e] = dequant_code(s_L, (q[e / 4] >> (8 * (e & 3))) & 0xFFu, d[e / Gm::kElems]);
-    if (full) {
-        float4* xp = reinterpret_cast<float4*>(a.x + base);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) st_cs(xp + i, make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]));
-    } else {
+        float x[kVec];
 #pragma unroll
         for (int e = 0; e < kVec; ++e)
-            if (base + e < a.n) a.x[base + e] = x[e];
+            x[e] = dequant_code(s_L, (q[c][e / 4] >> (8 * (e & 3))) & 0xFFu, d[e / Gm::kElems]);
+        if (full[c]) {
+            float4* xp = reinterpret_cast<float4*>(a.x + base[c]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                st_cs(xp + i, make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]));
+        } else {
+#pragma unroll
+            for (int e = 0; e < kVec; ++e)
+                if (base[c] + e < a.n) a.x[base[c] + e] = x[e];
+        }
     }
 }
 
@@ -351,8 +368,8 @@ cudaError_t launch_q(const QuantArgs& a, cudaStream_t s) {
 
 template <int G>
 cudaError_t launch_dq(const DequantArgs& a, cudaStream_t s) {
-    const int64_t threads = (a.n + kVec - 1) / kVec;
-    dre_dequantize_kernel<G><<<(unsigned)((threads + kThreads - 1) / kThreads), kThreads, 0, s>>>(a);
+    constexpr int64_t kCtaCodes = (int64_t)kDqChunks * kThreads * kVec;
+    dre_dequantize_kernel<G><<<(unsigned)((a.n + kCtaCodes - 1) / kCtaCodes), kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

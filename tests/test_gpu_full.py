@@ -33,7 +33,9 @@ def _bits(t: torch.Tensor) -> np.ndarray:
 
 
 @pytest.mark.parametrize("name,G,warm", [("olmo1b", 128, 20), ("llama7b", 128, 10),
-                                         ("llama13b", 16, 4), ("llama13b", 256, 4)])
+                                         ("llama13b", 16, 4), ("llama13b", 32, 4),
+                                         ("llama13b", 64, 4), ("llama13b", 128, 4),
+                                         ("llama13b", 256, 4)])
 def test_full_size_sampled(name, G, warm):
     dev = torch.device("cuda:0")
     wl = synth.workload(name, G)
