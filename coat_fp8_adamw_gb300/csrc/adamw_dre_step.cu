@@ -55,17 +55,10 @@ namespace coat {
 // [0] dequantized moments, [1] exponents k.  Only the rare path touches them.
 __device__ unsigned long long g_recompute[2];
 
-// The tables of the exact path, in global memory: only the few lanes that
-// re-evaluate candidates (and the per-group jobs) read them, through L1, so
-// the step kernel's shared memory can hold the inputs of that path instead.
-namespace gtab {
-#undef COAT_CONST
-#define COAT_CONST __device__
-#include "coat_tables.inc"
-#undef COAT_CONST
-#define COAT_CONST __constant__
-}  // namespace gtab
-
+// The exact path reads its tables from their global copies (gtab), through
+// L1: only the few lanes that re-evaluate candidates and the per-group jobs
+// read them, so the step kernel's shared memory holds that path's inputs
+// instead.
 __device__ __forceinline__ df::Tables global_tables() {
     return df::Tables{reinterpret_cast<const float*>(gtab::kLog2CenterHi),
                       reinterpret_cast<const float*>(gtab::kLog2CenterLo),
@@ -792,8 +785,8 @@ step_kernel_thread(const StepArgs a) {
     __shared__ float lg_hi[128], lg_lo[128];
     __shared__ SmemTables st;
     for (int i = threadIdx.x; i < 128; i += kThreadCta) {
-        lg_hi[i] = __uint_as_float(kLog2Frac448Hi[i]);
-        lg_lo[i] = __uint_as_float(kLog2Frac448Lo[i]);
+        lg_hi[i] = __uint_as_float(gtab::kLog2Frac448Hi[i]);
+        lg_lo[i] = __uint_as_float(gtab::kLog2Frac448Lo[i]);
     }
     load_smem_tables(st, threadIdx.x, kThreadCta);
     __syncthreads();

@@ -21,6 +21,17 @@
 
 namespace coat {
 
+// The same tables in global memory: filling shared-memory copies from these
+// is one coalesced load per warp, where reading constant memory with a
+// different index in every lane serializes the warp.
+namespace gtab {
+#undef COAT_CONST
+#define COAT_CONST __device__
+#include "coat_tables.inc"
+#undef COAT_CONST
+#define COAT_CONST __constant__
+}  // namespace gtab
+
 constexpr int kVec = 16;         // elements per thread: one 128-bit load of codes
 constexpr int kThreads = 256;    // threads per CTA
 
@@ -107,12 +118,12 @@ struct SmemTables {
 
 __device__ __forceinline__ void load_smem_tables(SmemTables& st, int tid, int nthreads) {
     for (int i = tid; i < 64; i += nthreads) {
-        st.log2c_hi[i] = __uint_as_float(kLog2CenterHi[i]);
-        st.log2c_lo[i] = __uint_as_float(kLog2CenterLo[i]);
+        st.log2c_hi[i] = __uint_as_float(gtab::kLog2CenterHi[i]);
+        st.log2c_lo[i] = __uint_as_float(gtab::kLog2CenterLo[i]);
     }
     for (int i = tid; i < 33; i += nthreads) {
-        st.exp2j_hi[i] = __uint_as_float(kExp2FracHi[i]);
-        st.exp2j_lo[i] = __uint_as_float(kExp2FracLo[i]);
+        st.exp2j_hi[i] = __uint_as_float(gtab::kExp2FracHi[i]);
+        st.exp2j_lo[i] = __uint_as_float(gtab::kExp2FracLo[i]);
     }
 }
 

@@ -151,6 +151,7 @@ struct DequantGroup {
     float Pm;
     int Pe;
     float rk_hi, rk_lo;
+    float P;   // Pm 2^Pe when that is a normal float, else 0 (the split path decides)
 };
 
 __device__ __forceinline__ DequantGroup dequant_group(float S, float k, const df::Tables& t) {
@@ -161,31 +162,43 @@ __device__ __forceinline__ DequantGroup dequant_group(float S, float k, const df
     if (!(S > 0.0f)) {
         d.Pm = 0.0f;
         d.Pe = 0;
+        d.P = 0.0f;
         return d;
     }
     const df::F2 z = df::mul22(df::add2(df::log2_df(S, t), const_df(kLog2_448Df)), rkd);
     const float n0 = rintf(z.hi);
     d.Pm = df::exp2_df(df::F2{__fsub_rn(z.hi, n0), z.lo}, t);
     d.Pe = (int)n0;
+    d.P = (d.Pe >= -125 && d.Pe <= 126) ? df::scale2(d.Pm, d.Pe) : 0.0f;
     return d;
 }
 
-// One code: sign(q) (|E4M3(q)| S)^(1/k) = sign(q) Pm 2^Pe 2^(L / k) with
-// L = log2(|E4M3(q)| / 448) from the double-float table.  L / k is formed as
-// a double-float product, its integer part n is applied exactly and only the
-// fraction f (|f| <= 1/2) goes through the SFU exp2 (relative error <= 2^-22
-// there), so the result is within about 2^-22 + 2^-23 of the exact value.  A
-// result outside the normal fp32 range is scaled with one more rounding.
+// One code: sign(q) (|E4M3(q)| S)^(1/k) = sign(q) P 2^(L / k) with
+// L = log2(|E4M3(q)| / 448) from the double-float table, |L / k| <= 17.8 / k.
+// p = RN(L_hi / k) goes through the SFU exp2 (relative error <= 2^-22 for
+// these arguments) and the rest of the double-float exponent, t (|t| <~ 2^-20),
+// corrects it to first order: P (y + y t ln 2), y = 2^p.  The result is within
+// about 2^-22 + 3 2^-24 of the exact value, 4.5e-7 (the codec's bar is 1e-6).
+// When P is not a normal float (k < 1 with an extreme S) the group takes the
+// split form: the integer part of the exponent applied exactly, the fraction
+// through the SFU, a result outside the normal range scaled with one more
+// rounding.
 __device__ __forceinline__ float dequant_code(const float2* s_L, uint32_t code, const DequantGroup& d) {
     const uint32_t mag = code & 0x7Fu;
     if (mag == 0u || !(d.Pm > 0.0f)) return 0.0f;
     const float2 L = s_L[mag];
     const float p = __fmul_rn(L.x, d.rk_hi);
     const float t = fmaf(L.x, d.rk_lo, fmaf(L.y, d.rk_hi, fmaf(L.x, d.rk_hi, -p)));
-    const float n = rintf(p);
+    if (d.P > 0.0f) {
+        const float y = ex2_ftz(p);
+        const float x = __fmul_rn(d.P, fmaf(y, t * 0.693147182f, y));
+        return __uint_as_float(__float_as_uint(x) | ((code & 0x80u) << 24));
+    }
+    const float rr = __fadd_rn(p, 12582912.0f);          // 1.5 2^23: rounds p to an integer
+    const float n = __fsub_rn(rr, 12582912.0f);
     const float f = __fadd_rn(__fsub_rn(p, n), t);
     const float y = __fmul_rn(d.Pm, ex2_ftz(f));
-    const int ni = (int)n + d.Pe;
+    const int ni = (int)(__float_as_uint(rr) - 0x4B400000u) + d.Pe;
     const uint32_t yb = __float_as_uint(y);
     const int eb = (int)((yb >> 23) & 0xFFu) + ni;
     const float x = (eb >= 1 && eb <= 254) ? __uint_as_float(yb + ((uint32_t)ni << 23))
@@ -228,7 +241,8 @@ dre_dequantize_kernel(const DequantArgs a) {
         }
     }
     for (int i = threadIdx.x; i < 128; i += kThreads)
-        s_L[i] = make_float2(__uint_as_float(kLog2Frac448Hi[i]), __uint_as_float(kLog2Frac448Lo[i]));
+        s_L[i] = make_float2(__uint_as_float(gtab::kLog2Frac448Hi[i]),
+                             __uint_as_float(gtab::kLog2Frac448Lo[i]));
     load_smem_tables(st, threadIdx.x, kThreads);
     __syncthreads();
     const df::Tables tab = tables_of(st);
@@ -270,6 +284,71 @@ dre_dequantize_kernel(const DequantArgs a) {
 #pragma unroll
             for (int e = 0; e < kVec; ++e)
                 if (base[c] + e < a.n) a.x[base[c] + e] = x[e];
+        }
+    }
+}
+
+// G >= 16: the CTA's 8192 codes as 64 rows of 128; warp w takes rows
+// 8w .. 8w + 7 and each lane 4 consecutive codes of a row (one 32-bit load),
+// so every warp store writes 512 contiguous bytes (the outputs are 4 of the 5
+// bytes moved per code).  The groups' parameters are formed once per CTA, one
+// thread per group, and shared.
+constexpr int kDqRows = 64;
+constexpr int kDqCtaCodes = kDqRows * 128;
+
+template <int G>
+__global__ void __launch_bounds__(kThreads)
+dre_dequantize_rows_kernel(const DequantArgs a) {
+    static_assert(G >= kVec, "row layout for G >= 16");
+    constexpr int kGpc = kDqCtaCodes / G;   // groups per CTA
+    constexpr int kRowsPerWarp = kDqRows / (kThreads / 32);
+    __shared__ float2 s_L[128];
+    __shared__ SmemTables st;
+    __shared__ DequantGroup s_d[kGpc];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t cta0 = (int64_t)blockIdx.x * kDqCtaCodes;
+    // the codes first: in flight while the tables and the groups are set up
+    uint32_t q[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const int64_t b = cta0 + (int64_t)(warp * kRowsPerWarp + r) * 128 + 4 * lane;
+        if (b + 4 <= a.n) {
+            q[r] = __ldcs(reinterpret_cast<const unsigned int*>(a.q + b));
+        } else {
+            q[r] = 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (b + j < a.n) q[r] |= (uint32_t)a.q[b + j] << (8 * j);
+        }
+    }
+    for (int i = threadIdx.x; i < 128; i += kThreads)
+        s_L[i] = make_float2(__uint_as_float(gtab::kLog2Frac448Hi[i]),
+                             __uint_as_float(gtab::kLog2Frac448Lo[i]));
+    load_smem_tables(st, threadIdx.x, kThreads);
+    __syncthreads();
+    const df::Tables tab = tables_of(st);
+    const int64_t gcta = cta0 / G;
+    for (int j = threadIdx.x; j < kGpc; j += kThreads) {
+        float S = 0.0f, k = 1.0f;
+        if ((gcta + j) * G < a.n) { S = a.scale[gcta + j]; k = a.k[gcta + j]; }
+        s_d[j] = dequant_group(S, k, tab);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const int row = warp * kRowsPerWarp + r;
+        const int64_t b = cta0 + (int64_t)row * 128 + 4 * lane;
+        if (b >= a.n) break;
+        const DequantGroup& d = s_d[(row * 128 + 4 * lane) / G];
+        float x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = dequant_code(s_L, (q[r] >> (8 * j)) & 0xFFu, d);
+        if (b + 4 <= a.n) {
+            st_cs(reinterpret_cast<float4*>(a.x + b), make_float4(x[0], x[1], x[2], x[3]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (b + j < a.n) a.x[b + j] = x[j];
         }
     }
 }
@@ -368,8 +447,12 @@ cudaError_t launch_q(const QuantArgs& a, cudaStream_t s) {
 
 template <int G>
 cudaError_t launch_dq(const DequantArgs& a, cudaStream_t s) {
-    constexpr int64_t kCtaCodes = (int64_t)kDqChunks * kThreads * kVec;
-    dre_dequantize_kernel<G><<<(unsigned)((a.n + kCtaCodes - 1) / kCtaCodes), kThreads, 0, s>>>(a);
+    if constexpr (G >= kVec) {
+        dre_dequantize_rows_kernel<G><<<(unsigned)((a.n + kDqCtaCodes - 1) / kDqCtaCodes), kThreads, 0, s>>>(a);
+    } else {
+        constexpr int64_t kCtaCodes = (int64_t)kDqChunks * kThreads * kVec;
+        dre_dequantize_kernel<G><<<(unsigned)((a.n + kCtaCodes - 1) / kCtaCodes), kThreads, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 
