@@ -21,6 +21,7 @@ from . import _build
 __all__ = ["CoatError", "coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
            "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
            "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_act_quantize_fp8",
+           "coat_fp8_linear_group_quantize",
            "coat_dre_dequantize", "coat_exact_recompute_counts", "coat_status_string",
            "coat_r_e4m3", "coat_version", "lib",
            "lib_path", "num_groups", "bytes_per_param", "STATUS",
@@ -40,6 +41,7 @@ MAX_N = 1 << 40
 EXPORTS = ("coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
            "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
            "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_act_quantize_fp8",
+           "coat_fp8_linear_group_quantize",
            "coat_dre_dequantize", "coat_exact_recompute_counts", "coat_status_string",
            "coat_r_e4m3", "coat_version")
 
@@ -88,6 +90,9 @@ def lib() -> ctypes.CDLL:
         L.coat_fp8_quantize_absmax.restype = ctypes.c_int
         L.coat_act_quantize_fp8.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp]
         L.coat_act_quantize_fp8.restype = ctypes.c_int
+        L.coat_fp8_linear_group_quantize.argtypes = [vp, f32, vp, f32, i64, i64, i64, i32, vp, vp,
+                                                     vp, vp]
+        L.coat_fp8_linear_group_quantize.restype = ctypes.c_int
         L.coat_dre_dequantize.argtypes = [vp, vp, vp, i64, i32, vp, vp]
         L.coat_dre_dequantize.restype = ctypes.c_int
         L.coat_exact_recompute_counts.argtypes = [vp, i32]
@@ -304,6 +309,27 @@ def coat_act_quantize_fp8(x, G: int, q, scale, qt=None, stream=None) -> None:
         st = lib().coat_act_quantize_fp8(px, M, N, int(G), pq, pqt, ps, _stream_ptr(stream))
     if st != 0:
         raise CoatError(st, "coat_act_quantize_fp8")
+
+
+def coat_fp8_linear_group_quantize(xq, sx: float, wq, sw: float, G: int, q, scale, y=None,
+                                   stream=None) -> None:
+    """FP8 linear layer with a per-group FP8 output: y = (sx E4M3(xq)) (sw E4M3(wq))^T
+    for xq uint8 [M, K] and wq uint8 [N, K], quantized per 1 x G group of each row
+    into q uint8 [M, N] and scale fp32 [M, N/G]; y fp32 [M, N] is written when given."""
+    import torch
+    if xq.dim() != 2 or wq.dim() != 2 or xq.shape[1] != wq.shape[1]:
+        raise ValueError("xq [M, K] and wq [N, K] must be 2-D with the same K")
+    (M, K), N = xq.shape, wq.shape[0]
+    px = _check(xq, torch.uint8, M * K, "xq")
+    pw = _check(wq, torch.uint8, N * K, "wq", xq.device)
+    pq = _check(q, torch.uint8, M * N, "q", xq.device)
+    ps = _check(scale, torch.float32, (M * N) // G if G > 0 else 0, "scale", xq.device)
+    py = _check(y, torch.float32, M * N, "y", xq.device) if y is not None else None
+    with torch.cuda.device(xq.device):
+        st = lib().coat_fp8_linear_group_quantize(px, float(sx), pw, float(sw), M, N, K, int(G),
+                                                  pq, ps, py, _stream_ptr(stream))
+    if st != 0:
+        raise CoatError(st, "coat_fp8_linear_group_quantize")
 
 
 def coat_dre_dequantize(q, scale, k, G: int, x, stream=None) -> None:

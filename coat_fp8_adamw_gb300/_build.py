@@ -19,7 +19,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_NAME = "libcoat_gb300.so"
 SOURCES = ("coat_abi.cu", "adamw_dre_step.cu", "dre_codec.cu", "act_quant.cu", "host_stream.cu",
-           "host_static.cu")
+           "host_static.cu", "linear_fp8.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
               "--expt-relaxed-constexpr"]

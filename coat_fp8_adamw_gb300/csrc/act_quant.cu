@@ -147,6 +147,8 @@ act_quant_kernel(const ActArgs a) {
                 }
             }
         }
+        codes[0] = e4m3_canonical_zero(codes[0]);
+        codes[1] = e4m3_canonical_zero(codes[1]);
         const int tr = 8 * p + r_in;
         tile[tr * kPitchW + c8 / 4] = codes[0];
         tile[tr * kPitchW + c8 / 4 + 1] = codes[1];

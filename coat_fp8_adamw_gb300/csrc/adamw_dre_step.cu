@@ -755,7 +755,8 @@ step_kernel_cta(const StepArgs a) {
             const int slot = chunk_slot(tid, q);
             const float4 m4 = *reinterpret_cast<const float4*>(&sm_m[tid][slot]);
             const float4 v4 = *reinterpret_cast<const float4*>(&sm_v[tid][slot]);
-            om[q] = encode_pair_m(m4.x, m4.y, km, invm, czm) | (encode_pair_m(m4.z, m4.w, km, invm, czm) << 16);
+            om[q] = e4m3_canonical_zero(encode_pair_m(m4.x, m4.y, km, invm, czm) |
+                                        (encode_pair_m(m4.z, m4.w, km, invm, czm) << 16));
             ov[q] = encode_pair_v(v4.x, v4.y, kv, invv, czv) | (encode_pair_v(v4.z, v4.w, kv, invv, czv) << 16);
         }
         if (full) {
@@ -865,7 +866,7 @@ step_kernel_thread(const StepArgs a) {
         const float ym1 = copysignf(ex2_ftz(fmaf(km[j1], lg2_ftz(fabsf(m[e + 1]) * inv_m[j1]), cz_m[j1])), m[e + 1]);
         const float yv0 = ex2_ftz(fmaf(kv[j0], lg2_ftz(v[e] * inv_v[j0]), cz_v[j0]));
         const float yv1 = ex2_ftz(fmaf(kv[j1], lg2_ftz(v[e + 1] * inv_v[j1]), cz_v[j1]));
-        const uint32_t pm_ = e4m3x2(ym0, ym1), pv_ = e4m3x2(yv0, yv1);
+        const uint32_t pm_ = e4m3_canonical_zero(e4m3x2(ym0, ym1)), pv_ = e4m3x2(yv0, yv1);
         if ((e & 2) == 0) { om[e / 4] = pm_; ov[e / 4] = pv_; }
         else { om[e / 4] |= pm_ << 16; ov[e / 4] |= pv_ << 16; }
     }

@@ -174,6 +174,33 @@ coat_status coat_act_quantize_fp8(const uint16_t* x, int64_t M, int64_t N, int32
     return from_cuda(coat::launch_act_quant(a, G, static_cast<cudaStream_t>(stream)));
 }
 
+coat_status coat_fp8_linear_group_quantize(const uint8_t* xq, float sx, const uint8_t* wq,
+                                           float sw, int64_t M, int64_t N, int64_t K, int32_t G,
+                                           uint8_t* q, float* scale, float* y, void* stream) {
+    if (!xq || !wq || !q || !scale || M < 1 || N < 1 || K < 1) return COAT_ERR_INVALID_ARG;
+    if (!(sx > 0.0f) || !(sw > 0.0f) || !std::isfinite(sx) || !std::isfinite(sw))
+        return COAT_ERR_INVALID_ARG;
+    if (G < 8 || G > 128 || (G & (G - 1)) != 0) return COAT_ERR_UNSUPPORTED_G;
+    if (M % 128 != 0 || N % 128 != 0 || K % 64 != 0) return COAT_ERR_INVALID_ARG;
+    if (M / 128 > 65535 || N / 128 >= (1LL << 31) || K > (1LL << 40) / N) return COAT_ERR_INVALID_ARG;
+    if (!aligned16(xq) || !aligned16(wq) || !aligned16(q) || !aligned16(scale) || (y && !aligned16(y)))
+        return COAT_ERR_MISALIGNED;
+    const size_t nx = (size_t)M * (size_t)K, nw = (size_t)N * (size_t)K;
+    const size_t ny = (size_t)M * (size_t)N, ns = 4 * (ny / (size_t)G);
+    const void* out[3] = {q, scale, y};
+    const size_t nout[3] = {ny, ns, 4 * ny};
+    for (int i = 0; i < 3; ++i) {
+        if (!out[i]) continue;
+        if (overlaps(out[i], nout[i], xq, nx) || overlaps(out[i], nout[i], wq, nw)) return COAT_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 3; ++j)
+            if (out[j] && overlaps(out[i], nout[i], out[j], nout[j])) return COAT_ERR_INVALID_ARG;
+    }
+    if (!is_device(xq) || !is_device(wq) || !is_device(q) || !is_device(scale) || (y && !is_device(y)))
+        return COAT_ERR_NOT_DEVICE;
+    coat::LinArgs a{xq, wq, sx, sw, M, N, K, q, scale, y};
+    return from_cuda(coat::launch_linear_fp8(a, G, static_cast<cudaStream_t>(stream)));
+}
+
 coat_status coat_dre_dequantize(const uint8_t* q, const float* scale, const float* k, int64_t n,
                                 int32_t G, float* x, void* stream) {
     if (!x || !q || !scale || !k || !size_ok(n)) return COAT_ERR_INVALID_ARG;

@@ -212,6 +212,16 @@ static __device__ __noinline__ uint32_t e4m3_code_of_quotient_exact(float x, flo
     return e4m3x2(__fadd_rn(e4m3_quotient(x, S), 0.0f), 0.0f) & 0xFFu;
 }
 
+// The stored code of a zero is 0x00 whatever the sign of the value that
+// rounded to it: the conversion gives 0x80 for a negative value below half the
+// smallest subnormal, and this clears the sign bit of every byte of a packed
+// word whose low seven bits are all zero (bit 7 of (b & 0x7F) + 0x7F is set
+// exactly when b & 0x7F is not zero; no byte carries into the next).
+__device__ __forceinline__ uint32_t e4m3_canonical_zero(uint32_t w) {
+    const uint32_t nz = (w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu;
+    return w & (nz | 0x7F7F7F7Fu);
+}
+
 // Smallest-non-zero tracking: fp32 magnitudes as unsigned bits minus one, so
 // that zero wraps to 0xFFFFFFFF and never wins a min.
 __device__ __forceinline__ uint32_t nz_key(float a) { return __float_as_uint(a) - 1u; }

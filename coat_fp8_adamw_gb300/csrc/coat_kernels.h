@@ -69,7 +69,18 @@ struct ActArgs {
     float* scale;        // M x N/G
 };
 
+struct LinArgs {
+    const uint8_t* xq;   // M x K E4M3 codes, row-major
+    const uint8_t* wq;   // N x K E4M3 codes, row-major
+    float sx, sw;        // per-tensor scales of X and W
+    int64_t M, N, K;
+    uint8_t* q;          // M x N output codes
+    float* scale;        // M x N/G output group scales
+    float* y;            // M x N float32 output before quantization (may be null)
+};
+
 cudaError_t launch_dre_quantize(const QuantArgs& a, int G, cudaStream_t stream);
+cudaError_t launch_linear_fp8(const LinArgs& a, int G, cudaStream_t stream);
 cudaError_t launch_act_quant(const ActArgs& a, int G, cudaStream_t stream);
 cudaError_t launch_absmax_quantize(const QuantArgs& a, int G, cudaStream_t stream);
 cudaError_t launch_dre_dequantize(const DequantArgs& a, int G, cudaStream_t stream);

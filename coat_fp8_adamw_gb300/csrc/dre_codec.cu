@@ -125,6 +125,8 @@ dre_quantize_kernel(const QuantArgs a) {
         const uint32_t p = e4m3x2(expand_scaled(x[e], r0, qp[j0].k), expand_scaled(x[e + 1], r1, qp[j1].k));
         if ((e & 2) == 0) out[e / 4] = p; else out[e / 4] |= p << 16;
     }
+#pragma unroll
+    for (int i = 0; i < kVec / 4; ++i) out[i] = e4m3_canonical_zero(out[i]);
     if (full) {
         st_cs(reinterpret_cast<uint4*>(a.q + base), make_uint4(out[0], out[1], out[2], out[3]));
     } else {
@@ -415,6 +417,8 @@ absmax_quantize_kernel(const QuantArgs a) {
             }
         }
     }
+#pragma unroll
+    for (int i = 0; i < kVec / 4; ++i) out[i] = e4m3_canonical_zero(out[i]);
     if (full) {
         st_cs(reinterpret_cast<uint4*>(a.q + base), make_uint4(out[0], out[1], out[2], out[3]));
     } else {

@@ -296,6 +296,17 @@ def adamw_like_moments_torch(n: int, G: int, seed: int, device):
     return m.float(), v.float()
 
 
+def fp8_operand_codes_np(rows: int, cols: int, seed: int) -> np.ndarray:
+    """E4M3 codes of a per-tensor-quantized linear-layer operand, uint8 [rows, cols]:
+    a random sign and a magnitude code drawn around 0x58 (the value 16) with a
+    spread of 10 codes (about 1.25 binades), clipped to the finite codes 0..0x7E,
+    so that the largest values come near 448 as after an absmax scaling."""
+    rng = np.random.default_rng([seed, 17])
+    mag = np.clip(np.rint(rng.normal(88.0, 10.0, (rows, cols))), 0, 126).astype(np.uint8)
+    sign = (rng.random((rows, cols)) < 0.5).astype(np.uint8) << 7
+    return mag | sign
+
+
 def sample_groups(num_groups: int, count: int, seed: int) -> np.ndarray:
     """Sorted sample of group indices: the first, the last and ``count`` random ones."""
     rng = np.random.default_rng([seed, 99])

@@ -26,7 +26,8 @@
  *   that S stays a normal float in [2^-125, 2^126], rounds k to float, sets
  *   S = max|X|^k / 448 and encodes y = 448 sign(x) (|x|/max|X|)^k with
  *   round-to-nearest-even onto the E4M3 grid, saturating at +-448 (0x7E /
- *   0xFE); zero encodes as 0x00.  An all-zero group has S = 0, k = 1; a group
+ *   0xFE); a value that rounds to zero, of either sign, encodes as 0x00
+ *   (never 0x80), here and in every quantizer below.  An all-zero group has S = 0, k = 1; a group
  *   with one non-zero magnitude has k = 1.  R_E4M3 = 448 / 2^-9 = 229376
  *   (see coat_r_e4m3()).
  *
@@ -229,6 +230,31 @@ coat_status coat_fp8_quantize_absmax(const float *x, int64_t n, int32_t G, uint8
  */
 coat_status coat_act_quantize_fp8(const uint16_t *x, int64_t M, int64_t N, int32_t G, uint8_t *q,
                                   uint8_t *qt, float *scale, void *stream);
+
+/*
+ * FP8 linear layer whose output is already the next layer's per-group FP8
+ * activation (COAT review page, section 3: "mixed-granularity activation
+ * quantization" gives linear layers per-tensor FP8 inputs; "Triton kernels",
+ * linear layer optimisation, quantizes the GEMM's output tile per 1 x G group
+ * in the epilogue).
+ *   xq [M x K] uint8 E4M3 codes in, row-major, X = sx E4M3(xq);
+ *   wq [N x K] uint8 E4M3 codes in, row-major (the weight as stored by a
+ *      linear layer, out_features x in_features), W = sw E4M3(wq);
+ *   y = X W^T accumulated in float32 on the tensor cores, one float32 product
+ *      by RN(sx sw) at the end;
+ *   per row, per group of G consecutive columns: scale = RN(max|y| / 448),
+ *      q = E4M3(y / scale) (nearest even of the exact quotient, saturating);
+ *      a group of zeros has scale 0 and zero codes;
+ *   q [M x N] uint8 out;  scale [M x N/G] float32 out (group g of row r at
+ *      r*N/G + g);  y [M x N] float32 out, or NULL to skip writing it.
+ * sx, sw finite and > 0; G a power of two in [8, 128]; M and N multiples of
+ * 128, M <= 8,388,480; K a multiple of 64.  All pointers 16-byte aligned
+ * device memory of the current device; the outputs overlap neither the
+ * inputs nor each other.  Asynchronous on `stream`.
+ */
+coat_status coat_fp8_linear_group_quantize(const uint8_t *xq, float sx, const uint8_t *wq, float sw,
+                                           int64_t M, int64_t N, int64_t K, int32_t G, uint8_t *q,
+                                           float *scale, float *y, void *stream);
 
 /*
  * Inverse of coat_dre_quantize: x = sign(q) (|E4M3(q)| scale)^(1/k).

@@ -33,11 +33,21 @@ def code_ordinal(c: np.ndarray) -> np.ndarray:
 
 
 def compare_codes(gpu: np.ndarray, ref: np.ndarray, what: str) -> dict:
+    """Codes within one E4M3 step of the oracle's, few of them off; a zero is
+    always stored as 0x00, never 0x80."""
+    assert not (gpu == 0x80).any(), f"{what}: a zero stored as 0x80"
     d = np.abs(code_ordinal(gpu) - code_ordinal(ref))
     frac = float((d > 0).mean()) if d.size else 0.0
     assert d.size == 0 or d.max() <= 1, f"{what}: a code differs by {d.max()} E4M3 steps"
     assert frac <= CODE_FLIP_FRAC, f"{what}: {frac:.3e} of codes differ (> {CODE_FLIP_FRAC})"
     return {"flip_frac": frac, "flips": int((d > 0).sum())}
+
+
+def assert_codes_equal(gpu: np.ndarray, ref: np.ndarray, what: str) -> None:
+    """Bit-identical codes (the quantizers whose input is the oracle's own)."""
+    bad = np.nonzero(gpu.ravel() != ref.ravel())[0]
+    assert bad.size == 0, (f"{what}: {bad.size} codes differ, first at {bad[:4].tolist()}: "
+                           f"{gpu.ravel()[bad[:4]].tolist()} vs {ref.ravel()[bad[:4]].tolist()}")
 
 
 def compare_w(gpu: np.ndarray, ref: np.ndarray, what: str = "w") -> dict:

@@ -127,3 +127,20 @@ def test_absmax_quantizer_validation(L):
     assert L.coat_fp8_quantize_absmax(A + 4, 16, 16, A + 4096, A + 8192, None) == 2
     assert L.coat_fp8_quantize_absmax(A, 64, 16, A + 16, A + 8192, None) == 1   # x overlaps q
     assert L.coat_fp8_quantize_absmax(A, 64, 16, A + 4096, A + 8192, None) == 5
+
+
+def _lin(L, xq=A, sx=1.0, wq=A + 0x100000, sw=1.0, M=128, N=128, K=64, G=16, q=A + 0x200000,
+         S=A + 0x300000, y=None):
+    return L.coat_fp8_linear_group_quantize(xq, sx, wq, sw, M, N, K, G, q, S, y, None)
+
+
+def test_linear_validation(L):
+    assert _lin(L, xq=0) == 1
+    assert _lin(L, sx=0.0) == 1 and _lin(L, sw=-1.0) == 1 and _lin(L, sx=float("inf")) == 1
+    assert _lin(L, G=4) == 3 and _lin(L, G=256) == 3 and _lin(L, G=24) == 3
+    assert _lin(L, M=64) == 1 and _lin(L, N=192) == 1 and _lin(L, K=96) == 1
+    assert _lin(L, M=128 * 65536) == 1                       # grid rows
+    assert _lin(L, q=A + 0x200008) == 2 and _lin(L, y=A + 0x400004) == 2
+    assert _lin(L, q=A + 0x100000) == 1                      # q overlaps wq
+    assert _lin(L, y=A + 0x300000) == 1                      # y overlaps the scales
+    assert _lin(L) == 5 and _lin(L, y=A + 0x400000) == 5      # not device memory here

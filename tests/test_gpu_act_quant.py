@@ -47,7 +47,7 @@ def test_matches_oracle(G, shape):
     q, qt, S = _gpu(bits, G)
     qo, qto, So = oracle.act_quantize(bits, G)
     assert np.array_equal(S, So), "scales must be bit-identical"
-    P.compare_codes(q.ravel(), qo.ravel(), f"q G={G} {shape}")
+    P.assert_codes_equal(q, qo, f"q G={G} {shape}")
     assert np.array_equal(qt, q.T), "the second output is the first one transposed"
 
 
@@ -57,7 +57,7 @@ def test_ragged_column_tile_and_no_transpose():
     q, _, S = _gpu(bits, G, transposed=False)
     qo, _, So = oracle.act_quantize(bits, G)
     assert np.array_equal(S, So)
-    P.compare_codes(q.ravel(), qo.ravel(), "ragged q")
+    P.assert_codes_equal(q, qo, "ragged q")
     q2, qt2, _ = _gpu(bits, G)
     assert np.array_equal(q2, q) and np.array_equal(qt2, q.T)
 
@@ -75,7 +75,7 @@ def test_large_tensor_sampled_rows():
     bits = x[rows].view(torch.int16).cpu().numpy().view(np.uint16)
     qo, _, So = oracle.act_quantize(bits, G)
     assert np.array_equal(S[rows].cpu().numpy(), So)
-    P.compare_codes(q[rows].cpu().numpy().ravel(), qo.ravel(), "sampled rows")
+    P.assert_codes_equal(q[rows].cpu().numpy(), qo, "sampled rows")
     cols = np.sort(rng.choice(N, 64, replace=False))
     assert torch.equal(qt[cols], q[:, cols].T)
 

@@ -51,7 +51,7 @@ def test_absmax_quantizer_matches_oracle(G):
     q, S = _gpu_absmax(x, G)
     qo, So = oracle.absmax_quantize(x, G)
     assert np.array_equal(S, So), "scales must be bit-identical"
-    P.compare_codes(q, qo, f"absmax G={G}")
+    P.assert_codes_equal(q, qo, f"absmax G={G}")
 
 
 def _mse(x, back):
