@@ -22,7 +22,8 @@ __all__ = ["CoatError", "coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
            "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
            "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_act_quantize_fp8",
            "coat_fp8_linear_group_quantize",
-           "coat_dre_dequantize", "coat_exact_recompute_counts", "coat_status_string",
+           "coat_dre_dequantize", "coat_exact_recompute_counts", "coat_kernel_wait_timeouts",
+           "coat_status_string",
            "coat_r_e4m3", "coat_version", "lib",
            "lib_path", "num_groups", "bytes_per_param", "STATUS",
            "STATIC_SCRATCH_BYTES", "MAX_N"]
@@ -42,7 +43,8 @@ EXPORTS = ("coat_fp8_adamw_step", "coat_fp8_adamw_step_host",
            "coat_fp8_adamw_step_host_workspace_bytes", "coat_fp8_adamw_step_host_static",
            "coat_dre_quantize", "coat_fp8_quantize_absmax", "coat_act_quantize_fp8",
            "coat_fp8_linear_group_quantize",
-           "coat_dre_dequantize", "coat_exact_recompute_counts", "coat_status_string",
+           "coat_dre_dequantize", "coat_exact_recompute_counts", "coat_kernel_wait_timeouts",
+           "coat_status_string",
            "coat_r_e4m3", "coat_version")
 
 _lock = threading.Lock()
@@ -97,6 +99,8 @@ def lib() -> ctypes.CDLL:
         L.coat_dre_dequantize.restype = ctypes.c_int
         L.coat_exact_recompute_counts.argtypes = [vp, i32]
         L.coat_exact_recompute_counts.restype = ctypes.c_int
+        L.coat_kernel_wait_timeouts.argtypes = [vp, i32]
+        L.coat_kernel_wait_timeouts.restype = ctypes.c_int
         L.coat_status_string.argtypes = [ctypes.c_int]
         L.coat_status_string.restype = ctypes.c_char_p
         L.coat_r_e4m3.argtypes = []
@@ -119,6 +123,20 @@ def coat_exact_recompute_counts(reset: bool = False, device=None) -> tuple:
     if st != 0:
         raise CoatError(st, "coat_exact_recompute_counts")
     return int(out[0]), int(out[1])
+
+
+def coat_kernel_wait_timeouts(reset: bool = False, device=None) -> int:
+    """Bounded waits inside the library's pipelined kernels that gave up on
+    ``device`` (default: the current one) since load or the last reset; a
+    non-zero count means a launch returned unfinished.  Synchronizes."""
+    import torch
+    out = ctypes.c_uint64(0)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        st = lib().coat_kernel_wait_timeouts(ctypes.byref(out), int(bool(reset)))
+    if st != 0:
+        raise CoatError(st, "coat_kernel_wait_timeouts")
+    return int(out.value)
 
 
 def coat_status_string(status: int) -> str:

@@ -181,8 +181,8 @@ coat_status coat_fp8_linear_group_quantize(const uint8_t* xq, float sx, const ui
     if (!(sx > 0.0f) || !(sw > 0.0f) || !std::isfinite(sx) || !std::isfinite(sw))
         return COAT_ERR_INVALID_ARG;
     if (G < 8 || G > 128 || (G & (G - 1)) != 0) return COAT_ERR_UNSUPPORTED_G;
-    if (M % 128 != 0 || N % 128 != 0 || K % 64 != 0) return COAT_ERR_INVALID_ARG;
-    if (M / 128 > 65535 || N / 128 >= (1LL << 31) || K > (1LL << 40) / N) return COAT_ERR_INVALID_ARG;
+    if (N % 16 != 0 || N % G != 0 || K % 16 != 0) return COAT_ERR_INVALID_ARG;
+    if (M >= (1LL << 31) || N >= (1LL << 31) || K >= (1LL << 31)) return COAT_ERR_INVALID_ARG;
     if (!aligned16(xq) || !aligned16(wq) || !aligned16(q) || !aligned16(scale) || (y && !aligned16(y)))
         return COAT_ERR_MISALIGNED;
     const size_t nx = (size_t)M * (size_t)K, nw = (size_t)N * (size_t)K;
@@ -215,6 +215,14 @@ coat_status coat_dre_dequantize(const uint8_t* q, const float* scale, const floa
         return COAT_ERR_NOT_DEVICE;
     coat::DequantArgs a{q, scale, k, x, n};
     return from_cuda(coat::launch_dre_dequantize(a, G, static_cast<cudaStream_t>(stream)));
+}
+
+coat_status coat_kernel_wait_timeouts(uint64_t* count, int32_t reset) {
+    if (!count) return COAT_ERR_INVALID_ARG;
+    unsigned long long c = 0ull;
+    if (coat::read_wait_timeouts(&c, reset != 0) != cudaSuccess) return COAT_ERR_CUDA;
+    *count = c;
+    return COAT_OK;
 }
 
 coat_status coat_exact_recompute_counts(uint64_t counts[2], int32_t reset) {

@@ -81,6 +81,8 @@ struct LinArgs {
 
 cudaError_t launch_dre_quantize(const QuantArgs& a, int G, cudaStream_t stream);
 cudaError_t launch_linear_fp8(const LinArgs& a, int G, cudaStream_t stream);
+// bounded waits in the library's kernels that gave up, on the current device
+cudaError_t read_wait_timeouts(unsigned long long* out, bool reset);
 cudaError_t launch_act_quant(const ActArgs& a, int G, cudaStream_t stream);
 cudaError_t launch_absmax_quantize(const QuantArgs& a, int G, cudaStream_t stream);
 cudaError_t launch_dre_dequantize(const DequantArgs& a, int G, cudaStream_t stream);

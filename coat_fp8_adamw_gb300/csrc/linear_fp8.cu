@@ -11,173 +11,398 @@
 //   saturating, 0x00 for a quotient that rounds to zero (of either sign);
 //   an all-zero group gets S = 0 and zero codes.
 //
-// The contraction runs on the tensor cores through the warp-level FP8 MMA
-// (mma.sync m16n8k32, E4M3 x E4M3 -> fp32).  A CTA computes a 128 x 128
-// output tile: its 8 warps own 16 rows each across all 128 columns, so every
-// 1 x G group of a row lies in one warp and its maximum is a reduction over
-// the 4 lanes of a quad (two shuffles).  K advances in steps of 64 through two
-// shared-memory stages filled by cp.async; rows are padded to 80 bytes so
-// that the 32-bit fragment loads of a warp hit 32 distinct banks.
+// Blackwell organisation: a persistent kernel, one CTA per SM, walks the
+// 128 x 256 output tiles.  Warp 0 streams 128 x 128-byte tiles of X and
+// 256 x 128-byte tiles of W into a 4-stage shared-memory ring with TMA
+// (128-byte swizzle); warp 1 issues the fifth-generation tensor-core MMA
+// (tcgen05.mma kind::f8f6f4, M = 128, N = 256, K = 32, E4M3 x E4M3 -> f32)
+// into one of two 256-column accumulators in tensor memory; warps 4-7 read
+// the other accumulator back (tcgen05.ld, one output row per thread, so a
+// 1 x G group lies in one thread's registers) and run the scale-and-quantize
+// epilogue while the next tile accumulates.  Every wait on an mbarrier is
+// bounded: when one gives up, the kernel counts it in g_wait_timeouts, lets
+// its copies and MMAs in flight finish, frees its tensor memory and returns.
 #include <cstdint>
+#include <cuda.h>   // CUtensorMap and its enums; the encoder is fetched at run time
 
 #include "coat_device.cuh"
 #include "coat_kernels.h"
 
 namespace coat {
 
+__device__ unsigned long long g_wait_timeouts;
+
 namespace {
 
-constexpr int kLBM = 128;                 // CTA tile rows (M)
-constexpr int kLBN = 128;                 // CTA tile columns (N)
-constexpr int kLBK = 64;                  // K per stage (bytes of a row)
-constexpr int kLPitch = kLBK + 16;        // padded shared-memory row, bytes
-constexpr int kLThreads = 256;            // 8 warps x 16 rows
-constexpr int kLStage = kLBM * kLPitch;   // bytes of one operand stage
+constexpr int kBM = 128;                       // tile rows (M), the MMA's M
+constexpr int kBN = 256;                       // tile columns (N), the MMA's N
+constexpr int kBK = 128;                       // K bytes per stage: one 128-byte swizzle row
+constexpr int kMmaK = 32;                      // K of one kind::f8f6f4 MMA
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK;             // 16 KB
+constexpr int kBBytes = kBN * kBK;             // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 2 * kBN;        // two accumulators of 256 f32 columns
+constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kNumBars = 2 * kStages + 5;      // full, empty, acc full x2, acc empty x2, done
+constexpr int kSmemBytes = kBarOff + 8 * kNumBars + 16 + 1024;   // + slack for 1024-B alignment
+constexpr uint32_t kSpinLimit = 1u << 26;
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// Instruction descriptor of the MMA: D in f32 (bits 4-5 = 1), A and B E4M3
+// (bits 7-9 and 10-12 = 0), both K-major (bits 15, 16 = 0), N / 8 in bits
+// 17-22, M / 16 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 
-// four 8 x 16-byte shared-memory matrices; lanes 8 i .. 8 i + 7 give the row
-// addresses of matrix i, and lane l receives bytes 4 (l % 4) .. 4 (l % 4) + 3
-// of row l / 4 of each (the m16n8k32 E4M3 fragment layout)
-__device__ __forceinline__ void ldsm_x4(const unsigned char* p, uint32_t& r0, uint32_t& r1,
-                                        uint32_t& r2, uint32_t& r3) {
-    const uint32_t s = (uint32_t)__cvta_generic_to_shared(p);
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(s));
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// D += A B for a 16 x 32 E4M3 A (row-major fragment), a 32 x 8 E4M3 B
-// (column-major fragment) and a 16 x 8 fp32 accumulator.
-__device__ __forceinline__ void mma_e4m3(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+// ---- mbarriers ----
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
     asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+// Wait for the phase of parity `parity` to complete, at most kSpinLimit
+// polls; give up early once another role has aborted (when `abort` is given).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if (abort && (i & 255u) == 255u && *abort) return false;
+    }
+    atomicAdd(&g_wait_timeouts, 1ull);
+    if (abort) *abort = 1u;
+    return false;
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// one stage: rows [0, 128) of A (from row m0) and of B (from row n0), bytes
-// [k0, k0 + 64) of each row; 256 threads x 2 chunks of 16 bytes per operand
-__device__ __forceinline__ void load_stage(const LinArgs& a, unsigned char* sA, unsigned char* sB,
-                                           int64_t m0, int64_t n0, int64_t k0, int tid) {
+// ---- TMA ----
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// ---- tcgen05 ----
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout TMA writes: rows of 128 bytes, 8-row (1024-byte) swizzle
+// atoms.  Start address / 16 in bits 0-13, leading-dimension offset (unused
+// by this layout) in bits 16-29, stride between 8-row atoms / 16 in bits
+// 32-45, the descriptor version 1 in bits 46-47, swizzle mode 2 (128 bytes)
+// in bits 61-63.  A K offset inside the 128-byte row is added to the start
+// address: the swizzle is a function of the address bits.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+// arrive on `bar` once every MMA this thread issued before has completed
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x N consecutive 32-bit columns: thread i receives lane (taddr's lane + i)
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+        "%30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// One tile's epilogue for this thread's output row: per group of G columns,
+// the maximum of |y|, S, then the codes (and y when asked for).  Columns come
+// from tensor memory in chunks of up to 32; a group wider than a chunk is
+// read twice (maximum, then codes) instead of being held in registers.
+template <int G>
+__device__ __forceinline__ void epilogue_row(const LinArgs& a, uint32_t taddr, int64_t row, int64_t n0,
+                                             float sxw) {
+    constexpr int kCh = G < 32 ? G : 32;
+    constexpr int kNch = G / kCh;
+    const bool row_ok = row < a.M;
+    const int64_t ngr = a.N / G;
+#pragma unroll 1
+    for (int g = 0; g < kBN / G; ++g) {
+        const int64_t col0 = n0 + (int64_t)g * G;
+        if (col0 >= a.N) break;   // the same for the whole warp
+        uint32_t v[kCh];
+        float mx = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int c = tid + i * kLThreads;
-        const int row = c >> 2, col = (c & 3) * 16;
-        cp_async16(sA + row * kLPitch + col, a.xq + (m0 + row) * a.K + k0 + col);
-        cp_async16(sB + row * kLPitch + col, a.wq + (n0 + row) * a.K + k0 + col);
+        for (int c = 0; c < kNch; ++c) {
+            __syncwarp();   // tcgen05.ld is warp-collective: converge after the code branches
+            tmem_ld<kCh>(taddr + (uint32_t)(g * G + c * kCh), v);
+#pragma unroll
+            for (int e = 0; e < kCh; ++e) mx = fmaxf(mx, fabsf(__fmul_rn(__uint_as_float(v[e]), sxw)));
+        }
+        const float S = __fdiv_rn(mx, 448.0f);
+        const float inv = S > 0.0f ? rcp_approx(S) : 0.0f;
+        if (row_ok) a.scale[row * ngr + col0 / G] = S;
+#pragma unroll
+        for (int c = 0; c < kNch; ++c) {
+            if (kNch > 1) {
+                __syncwarp();
+                tmem_ld<kCh>(taddr + (uint32_t)(g * G + c * kCh), v);
+            }
+            float y[kCh];
+            uint32_t w[kCh / 4];
+#pragma unroll
+            for (int e = 0; e < kCh; ++e) y[e] = __fmul_rn(__uint_as_float(v[e]), sxw);
+#pragma unroll
+            for (int i = 0; i < kCh / 4; ++i) w[i] = 0u;
+            if (S > 0.0f) {
+#pragma unroll
+                for (int e = 0; e < kCh; ++e) {
+                    bool und;
+                    uint32_t code = e4m3_code_fast(y[e], inv, und);
+                    if (und) code = e4m3_code_of_quotient_exact(y[e], S);
+                    w[e / 4] |= code << (8 * (e & 3));
+                }
+            }
+            if (row_ok) {
+                uint8_t* qp = a.q + row * a.N + col0 + c * kCh;
+                if constexpr (kCh == 8) {
+                    *reinterpret_cast<uint2*>(qp) = make_uint2(e4m3_canonical_zero(w[0]), e4m3_canonical_zero(w[1]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kCh / 16; ++i)
+                        reinterpret_cast<uint4*>(qp)[i] =
+                            make_uint4(e4m3_canonical_zero(w[4 * i]), e4m3_canonical_zero(w[4 * i + 1]),
+                                       e4m3_canonical_zero(w[4 * i + 2]), e4m3_canonical_zero(w[4 * i + 3]));
+                }
+                if (a.y) {
+                    float4* yp = reinterpret_cast<float4*>(a.y + row * a.N + col0 + c * kCh);
+#pragma unroll
+                    for (int i = 0; i < kCh / 4; ++i)
+                        yp[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+                }
+            }
+        }
     }
 }
 
 template <int G>
-__global__ void __launch_bounds__(kLThreads, 2)
-linear_fp8_kernel(const LinArgs a) {
-    static_assert(G >= 8 && G <= kLBN && (kLBN % G) == 0, "G divides the tile");
-    __shared__ __align__(16) unsigned char sA[2][kLStage];
-    __shared__ __align__(16) unsigned char sB[2][kLStage];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gq = lane >> 2, tq = lane & 3;   // quad and lane within it
-    const int64_t m0 = (int64_t)blockIdx.y * kLBM, n0 = (int64_t)blockIdx.x * kLBN;
+__global__ void __launch_bounds__(kThreads, 1)
+linear_fp8_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+                  const LinArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // the 128-byte swizzle repeats every 1024 bytes: align the stages to it
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t bar0 = sb + kBarOff;
+    auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+    auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kStages + s); };
+    auto acc_full = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kStages + b); };
+    auto acc_empty = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kStages + 2 + b); };
+    const uint32_t done = bar0 + 8u * (uint32_t)(2 * kStages + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 8 * kNumBars);
+    volatile uint32_t* abort = tmem_slot + 1;
 
-    float acc[kLBN / 8][4];
-#pragma unroll
-    for (int j = 0; j < kLBN / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+        for (int b = 0; b < 2; ++b) { mbar_init(acc_full(b), 1); mbar_init(acc_empty(b), 128); }
+        mbar_init(done, 1);
+        *abort = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
-    const int64_t kt_n = a.K / kLBK;
-    load_stage(a, sA[0], sB[0], m0, n0, 0, tid);
-    cp_async_commit();
-    for (int64_t kt = 0; kt < kt_n; ++kt) {
-        const int s = (int)(kt & 1);
-        if (kt + 1 < kt_n) load_stage(a, sA[s ^ 1], sB[s ^ 1], m0, n0, (kt + 1) * kLBK, tid);
-        cp_async_commit();
-        cp_async_wait<1>();   // this stage has landed (the next may be in flight)
-        __syncthreads();
-        // A fragment rows: lanes 0-7 rows 0-7 and 8-15 rows 8-15 at k, lanes
-        // 16-31 the same rows at k + 16.  B: two n-blocks per ldmatrix, lanes
-        // 0-7 / 8-15 the first block at k / k + 16, lanes 16-31 the second.
-        const unsigned char* A = sA[s] + (warp * 16 + (lane & 15)) * kLPitch + (lane >> 4) * 16;
-        const unsigned char* B = sB[s] + ((lane & 7) + (lane >> 4) * 8) * kLPitch + ((lane >> 3) & 1) * 16;
-#pragma unroll
-        for (int kk = 0; kk < kLBK; kk += 32) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(A + kk, a0, a1, a2, a3);
-#pragma unroll
-            for (int j = 0; j < kLBN / 8; j += 2) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(B + 8 * j * kLPitch + kk, b0, b1, b2, b3);
-                mma_e4m3(acc[j], a0, a1, a2, a3, b0, b1);
-                mma_e4m3(acc[j + 1], a0, a1, a2, a3, b2, b3);
+    const int64_t num_m = (a.M + kBM - 1) / kBM, num_n = (a.N + kBN - 1) / kBN;
+    const int64_t tiles = num_m * num_n;
+    const int kblocks = (int)((a.K + kBK - 1) / kBK);
+
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer ----
+        int s = 0;
+        uint32_t ph = 0, issued = 0, last_ph = 0;   // per stage: issued at all, parity of the last issue
+        bool ok = true;
+        for (int64_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+            const int32_t m0 = (int32_t)((t % num_m) * kBM), n0 = (int32_t)((t / num_m) * kBN);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait(empty(s), ph ^ 1u, abort)) { ok = false; break; }
+                mbar_expect_tx(full(s), (uint32_t)kStageBytes);
+                const uint32_t sa = sb + (uint32_t)(s * kStageBytes);
+                tma_load_2d(sa, &tmx, kb * kBK, m0, full(s));
+                tma_load_2d(sa + kABytes, &tmw, kb * kBK, n0, full(s));
+                issued |= 1u << s;
+                last_ph = (last_ph & ~(1u << s)) | (ph << s);
+                if (++s == kStages) { s = 0; ph ^= 1u; }
             }
         }
-        __syncthreads();   // the stage is free for the load two steps on
-    }
-
-    // ---- epilogue: scale, per-group maximum, scale and codes ----
-    // This thread holds rows r0 and r0 + 8, columns 8 j + 2 tq + {0, 1}.
-    const float sxw = __fmul_rn(a.sx, a.sw);
-    const int64_t r0 = m0 + warp * 16 + gq;
-    const int64_t ngr = a.N / G;   // groups per output row
-    constexpr int kJ = G / 8;      // n-blocks per group
+        // every copy issued has landed before the CTA may exit
+        for (int i = 0; i < kStages; ++i)
+            if (issued & (1u << i)) mbar_wait(full(i), (last_ph >> i) & 1u, nullptr);
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer ----
+        int s = 0, acc = 0;
+        uint32_t ph = 0, aph = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+            if (!mbar_wait(acc_empty(acc), aph ^ 1u, abort)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * kBN);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait(full(s), ph, abort)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sa = sb + (uint32_t)(s * kStageBytes), sbb = sa + kABytes;
 #pragma unroll
-    for (int gi = 0; gi < kLBN / G; ++gi) {
-        float y[2][2 * kJ];
-        float mx0 = 0.0f, mx1 = 0.0f;
-#pragma unroll
-        for (int jj = 0; jj < kJ; ++jj) {
-            const int j = gi * kJ + jj;
-            y[0][2 * jj] = __fmul_rn(acc[j][0], sxw);
-            y[0][2 * jj + 1] = __fmul_rn(acc[j][1], sxw);
-            y[1][2 * jj] = __fmul_rn(acc[j][2], sxw);
-            y[1][2 * jj + 1] = __fmul_rn(acc[j][3], sxw);
-            mx0 = fmaxf(mx0, fmaxf(fabsf(y[0][2 * jj]), fabsf(y[0][2 * jj + 1])));
-            mx1 = fmaxf(mx1, fmaxf(fabsf(y[1][2 * jj]), fabsf(y[1][2 * jj + 1])));
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t row = r0 + 8 * h;
-            const float mx = h ? mx1 : mx0;
-            const float S = __fdiv_rn(mx, 448.0f);
-            const float inv = S > 0.0f ? rcp_approx(S) : 0.0f;
-            const int64_t gcol = n0 / G + gi;
-            if (tq == 0) a.scale[row * ngr + gcol] = S;
-#pragma unroll
-            for (int jj = 0; jj < kJ; ++jj) {
-                const int64_t col = n0 + gi * G + 8 * jj + 2 * tq;
-                uint32_t c2 = 0u;
-                if (S > 0.0f) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        bool und;
-                        uint32_t c = e4m3_code_fast(y[h][2 * jj + e], inv, und);
-                        if (und) c = e4m3_code_of_quotient_exact(y[h][2 * jj + e], S);
-                        c2 |= c << (8 * e);
-                    }
-                }
-                *reinterpret_cast<uint16_t*>(a.q + row * a.N + col) = (uint16_t)e4m3_canonical_zero(c2);
-                if (a.y)
-                    *reinterpret_cast<float2*>(a.y + row * a.N + col) =
-                        make_float2(y[h][2 * jj], y[h][2 * jj + 1]);
+                for (int kk = 0; kk < kBK / kMmaK; ++kk)
+                    mma_e4m3(d, sw128_desc(sa + kk * kMmaK), sw128_desc(sbb + kk * kMmaK), (kb | kk) != 0);
+                mma_commit(empty(s));   // the stage is free once these MMAs have read it
+                if (++s == kStages) { s = 0; ph ^= 1u; }
             }
+            if (!ok) break;
+            mma_commit(acc_full(acc));
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+        // every MMA issued has completed before tensor memory is freed
+        mma_commit(done);
+        mbar_wait(done, 0u, nullptr);
+    } else if (warp >= 4) {
+        // ---- epilogue: warp 4 + i reads tensor-memory lanes 32 i .. 32 i + 31 ----
+        const int q4 = warp & 3;
+        const float sxw = __fmul_rn(a.sx, a.sw);
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+            if (!mbar_wait(acc_full(acc), aph, abort)) break;
+            tc_fence_after();
+            const int64_t row = (t % num_m) * kBM + 32 * q4 + lane;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(acc * kBN);
+            epilogue_row<G>(a, taddr, row, (t / num_m) * kBN, sxw);
+            tc_fence_before();
+            mbar_arrive(acc_empty(acc));
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
         }
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                 CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static const EncodeTiled fn = []() -> EncodeTiled {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiled>(p);
+    }();
+    return fn;
+}
+
+// rows x K bytes, row-major; boxes of 128 bytes x box_rows rows, 128-byte swizzle,
+// zeros outside the tensor
+bool encode_operand(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K, uint32_t box_rows) {
+    const EncodeTiled fn = encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int G>
 cudaError_t launch_linear_g(const LinArgs& a, cudaStream_t s) {
-    const dim3 grid((unsigned)(a.N / kLBN), (unsigned)(a.M / kLBM));
-    linear_fp8_kernel<G><<<grid, kLThreads, 0, s>>>(a);
+    alignas(64) CUtensorMap tmx, tmw;
+    if (!encode_operand(&tmx, a.xq, a.M, a.K, kBM) || !encode_operand(&tmw, a.wq, a.N, a.K, kBN))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(linear_fp8_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
+    const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+    linear_fp8_kernel<G><<<grid, kThreads, kSmemBytes, s>>>(tmx, tmw, a);
     return cudaGetLastError();
 }
 
@@ -192,6 +417,13 @@ cudaError_t launch_linear_fp8(const LinArgs& a, int G, cudaStream_t s) {
         case 128: return launch_linear_g<128>(a, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t read_wait_timeouts(unsigned long long* out, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_wait_timeouts, sizeof(*out));
+    if (e != cudaSuccess || !reset) return e;
+    const unsigned long long zero = 0ull;
+    return cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(zero));
 }
 
 }  // namespace coat

@@ -247,10 +247,13 @@ coat_status coat_act_quantize_fp8(const uint16_t *x, int64_t M, int64_t N, int32
  *      a group of zeros has scale 0 and zero codes;
  *   q [M x N] uint8 out;  scale [M x N/G] float32 out (group g of row r at
  *      r*N/G + g);  y [M x N] float32 out, or NULL to skip writing it.
- * sx, sw finite and > 0; G a power of two in [8, 128]; M and N multiples of
- * 128, M <= 8,388,480; K a multiple of 64.  All pointers 16-byte aligned
- * device memory of the current device; the outputs overlap neither the
- * inputs nor each other.  Asynchronous on `stream`.
+ * sx, sw finite and > 0; G a power of two in [8, 128]; N a multiple of 16
+ * and of G; K a multiple of 16; M, N, K below 2^31 (M, N and K need not be
+ * multiples of the kernel's tiles).  All pointers 16-byte aligned device
+ * memory of the current device; the outputs overlap neither the inputs nor
+ * each other.  Asynchronous on `stream`.  The kernel waits on its own
+ * pipeline with bounded waits; a wait that gives up (which would be a bug)
+ * leaves the outputs unspecified and is counted by coat_kernel_wait_timeouts.
  */
 coat_status coat_fp8_linear_group_quantize(const uint8_t *xq, float sx, const uint8_t *wq, float sw,
                                            int64_t M, int64_t N, int64_t K, int32_t G, uint8_t *q,
@@ -280,6 +283,16 @@ coat_status coat_dre_dequantize(const uint8_t *q, const float *scale, const floa
  * a running step if exact counts are wanted.
  */
 coat_status coat_exact_recompute_counts(uint64_t counts[2], int32_t reset);
+
+/*
+ * How many bounded waits inside the library's kernels gave up on the current
+ * device since the library was loaded there (or since the last reset).  The
+ * pipelined kernels (coat_fp8_linear_group_quantize) wait on their own
+ * producers with an iteration limit instead of forever; a non-zero count
+ * means a launch returned without finishing its work.  reset != 0 clears the
+ * counter after reading it.  Synchronizes with the current device.
+ */
+coat_status coat_kernel_wait_timeouts(uint64_t *count, int32_t reset);
 
 /* Static description of a status code (never NULL). */
 const char *coat_status_string(coat_status status);

@@ -135,12 +135,14 @@ def _lin(L, xq=A, sx=1.0, wq=A + 0x100000, sw=1.0, M=128, N=128, K=64, G=16, q=A
 
 
 def test_linear_validation(L):
-    assert _lin(L, xq=0) == 1
+    assert _lin(L, xq=0) == 1 and _lin(L, M=0) == 1 and _lin(L, K=0) == 1
     assert _lin(L, sx=0.0) == 1 and _lin(L, sw=-1.0) == 1 and _lin(L, sx=float("inf")) == 1
     assert _lin(L, G=4) == 3 and _lin(L, G=256) == 3 and _lin(L, G=24) == 3
-    assert _lin(L, M=64) == 1 and _lin(L, N=192) == 1 and _lin(L, K=96) == 1
-    assert _lin(L, M=128 * 65536) == 1                       # grid rows
+    assert _lin(L, N=120) == 1 and _lin(L, N=48, G=32) == 1 and _lin(L, K=40) == 1
+    assert _lin(L, M=1 << 31) == 1                            # TMA coordinates are 32-bit
     assert _lin(L, q=A + 0x200008) == 2 and _lin(L, y=A + 0x400004) == 2
     assert _lin(L, q=A + 0x100000) == 1                      # q overlaps wq
     assert _lin(L, y=A + 0x300000) == 1                      # y overlaps the scales
     assert _lin(L) == 5 and _lin(L, y=A + 0x400000) == 5      # not device memory here
+    assert _lin(L, M=1, N=16, K=16) == 5                      # ragged sizes pass validation
+    assert L.coat_kernel_wait_timeouts(None, 0) == 1

@@ -6,7 +6,8 @@ COAT review page, section 3: linear layers take per-tensor FP8 inputs
 quantizes its output tile per 1 x G group ("Triton kernels", linear layer
 optimisation).
 
-The kernel accumulates in float32 on the tensor cores, so its y is not the
+The kernel runs on the fifth-generation tensor cores (TMA-fed shared-memory
+ring, accumulators in tensor memory) and accumulates in float32, so its y is not the
 oracle's correctly rounded one; the checks are
   * y within the float32 summation bound (K + 2) 2^-24 |sx sw| sum_k |x_k w_k|
     of the oracle's y (K - 1 additions, the product by RN(sx sw) and that
@@ -45,6 +46,7 @@ def _gpu(xq, sx, wq, sw, G, want_y=True):
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") if want_y else None
     coat.coat_fp8_linear_group_quantize(dx, sx, dw, sw, G, q, S, y)
     torch.cuda.synchronize()
+    assert coat.coat_kernel_wait_timeouts(reset=True) == 0, "a pipeline wait gave up"
     return (y.cpu().numpy() if want_y else None), q.cpu().numpy(), S.cpu().numpy()
 
 
@@ -86,6 +88,28 @@ def test_matches_oracle_over_several_tiles(G):
     y, q, S = _gpu(xq, sx, wq, sw, G)
     worst = _check(xq, sx, wq, sw, G, y, q, S)
     print(f"G={G}: worst |dy| = {worst:.3f} of the summation bound")
+
+
+@pytest.mark.parametrize("M,N,K,G", [(200, 272, 208, 16), (1, 16, 16, 16), (37, 48, 48, 8),
+                                     (129, 2064, 1040, 16), (300, 384, 4112, 128)])
+def test_ragged_shapes(M, N, K, G):
+    """Sizes that are not multiples of the 128 x 256 x 128 tiles: the loads
+    beyond the edges read zeros and the stores beyond them are skipped."""
+    xq = synth.fp8_operand_codes_np(M, K, M + 1)
+    wq = synth.fp8_operand_codes_np(N, K, N + 2)
+    y, q, S = _gpu(xq, 0.0173, wq, 0.0291, G)
+    _check(xq, 0.0173, wq, 0.0291, G, y, q, S)
+
+
+def test_more_tiles_than_sms():
+    """320 tiles: each persistent CTA takes two or three, alternating between
+    its two tensor-memory accumulators."""
+    M, N, K, G = 128 * 40, 256 * 8, 256, 32
+    xq = synth.fp8_operand_codes_np(M, K, 31)
+    wq = synth.fp8_operand_codes_np(N, K, 32)
+    y, q, S = _gpu(xq, 0.031, wq, 0.0047, G)
+    rows = np.unique(np.concatenate([np.arange(0, M, 97), [M - 1]]))
+    _check(xq, 0.031, wq, 0.0047, G, y[rows], q[rows], S[rows], rows=rows)
 
 
 def test_without_y_gives_the_same_codes():
