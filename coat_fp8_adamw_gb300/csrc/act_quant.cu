@@ -27,31 +27,6 @@ namespace coat {
 
 namespace {
 
-// Packed fp32 pairs (PTX .f32x2): each half rounds like the scalar instruction.
-__device__ __forceinline__ uint64_t pk(float x, float y) {
-    uint64_t u;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(x), "f"(y));
-    return u;
-}
-__device__ __forceinline__ void upk(uint64_t u, float& x, float& y) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(u));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
 // RN(m / 448) for a bf16 group maximum m >= 0: q = RN(m y) with y = RN(1/448),
 // then one FMA correction from the exact remainder m - q 448 (Markstein's
 // division by a known divisor).  Checked against the correctly rounded
@@ -63,9 +38,6 @@ __device__ __forceinline__ float div448_bf16(float m) {
     return fmaf(r, kInv448, q);
 }
 
-// y (1 - 2^-20) and y (1 + 2^-20): see e4m3_code_fast
-constexpr float kDn = 0.99999904632568359f;
-constexpr float kUp = 1.00000095367431641f;
 
 constexpr int kTileR = 64;                  // rows per tile
 constexpr int kTileC = 128;                 // columns per tile

@@ -84,6 +84,31 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
+// Packed fp32 pairs (PTX .f32x2): each half rounds like the scalar instruction.
+__device__ __forceinline__ uint64_t pk(float x, float y) {
+    uint64_t u;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(x), "f"(y));
+    return u;
+}
+__device__ __forceinline__ void upk(uint64_t u, float& x, float& y) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(u));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Two fp32 values -> two E4M3 codes (round to nearest even, saturate to
 // +-448), packed little-endian: lo -> bits 0..7, hi -> bits 8..15.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -201,9 +226,11 @@ __device__ __forceinline__ float e4m3_quotient(float x, float S) {
 // the exact quotient and that code is the answer.  The other elements (a
 // midpoint within a few steps, or an SFU reciprocal that is not finite) are
 // flagged in `undecided` and left to e4m3_code_of_quotient_exact.
+constexpr float kDn = 0.99999904632568359f;   // 1 - 2^-20
+constexpr float kUp = 1.00000095367431641f;   // 1 + 2^-20
 __device__ __forceinline__ uint32_t e4m3_code_fast(float x, float inv, bool& undecided) {
     const float y = fmaf(x, inv, 0.0f);   // +0 for a zero of either sign
-    const uint32_t p = e4m3x2(y * 0.99999904632568359f, y * 1.00000095367431641f);
+    const uint32_t p = e4m3x2(y * kDn, y * kUp);
     undecided = (p & 0xFFu) != (p >> 8) || !(inv <= 3.40282347e38f);
     return p & 0xFFu;
 }

@@ -11,17 +11,22 @@
 //   saturating, 0x00 for a quotient that rounds to zero (of either sign);
 //   an all-zero group gets S = 0 and zero codes.
 //
-// Blackwell organisation: a persistent kernel, one CTA per SM, walks the
-// 128 x 256 output tiles.  Warp 0 streams 128 x 128-byte tiles of X and
-// 256 x 128-byte tiles of W into a 4-stage shared-memory ring with TMA
-// (128-byte swizzle); warp 1 issues the fifth-generation tensor-core MMA
-// (tcgen05.mma kind::f8f6f4, M = 128, N = 256, K = 32, E4M3 x E4M3 -> f32)
-// into one of two 256-column accumulators in tensor memory; warps 4-7 read
-// the other accumulator back (tcgen05.ld, one output row per thread, so a
-// 1 x G group lies in one thread's registers) and run the scale-and-quantize
-// epilogue while the next tile accumulates.  Every wait on an mbarrier is
-// bounded: when one gives up, the kernel counts it in g_wait_timeouts, lets
-// its copies and MMAs in flight finish, frees its tensor memory and returns.
+// Blackwell organisation: persistent CTA pairs (clusters of two, one CTA per
+// SM) walk the 256 x 256 output tiles.  Each CTA streams its 128 rows of X and
+// its 128 rows of W (half the tile's columns) in 128-byte K slices into a
+// 6-stage shared-memory ring with TMA (128-byte swizzle), both signalling the
+// even CTA's barrier.  One thread of the even CTA issues the pair-wide
+// fifth-generation tensor-core MMA (tcgen05.mma.cta_group::2 kind::f8f6f4,
+// M = 256, N = 256, K = 32, E4M3 x E4M3 -> f32): each SM multiplies its own
+// 128 rows of X by both halves of W, so a CTA loads a third less per FLOP than
+// a single-SM 128 x 256 tile.  Accumulators alternate between two 256-column
+// halves of tensor memory; eight epilogue warps per CTA (two per SM
+// sub-partition, each taking 128 of the 256 columns) read their CTA's 128
+// rows back (tcgen05.ld, one output row per thread, so a 1 x G group lies in
+// one thread's registers) and run the scale-and-quantize epilogue while the
+// next tile accumulates.  Every wait on an mbarrier is bounded: when one gives up,
+// the kernel counts it in g_wait_timeouts, lets its copies and MMAs in flight
+// finish, frees its tensor memory and returns.
 #include <cstdint>
 #include <cuda.h>   // CUtensorMap and its enums; the encoder is fetched at run time
 
@@ -34,25 +39,28 @@ __device__ unsigned long long g_wait_timeouts;
 
 namespace {
 
-constexpr int kBM = 128;                       // tile rows (M), the MMA's M
-constexpr int kBN = 256;                       // tile columns (N), the MMA's N
+constexpr int kBM = 128;                       // rows of X per CTA (the pair's MMA has M = 256)
+constexpr int kBN = 256;                       // tile columns (N) = the MMA's N
+constexpr int kBNh = kBN / 2;                  // rows of W per CTA
 constexpr int kBK = 128;                       // K bytes per stage: one 128-byte swizzle row
 constexpr int kMmaK = 32;                      // K of one kind::f8f6f4 MMA
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kABytes = kBM * kBK;             // 16 KB
-constexpr int kBBytes = kBN * kBK;             // 32 KB
+constexpr int kBBytes = kBNh * kBK;            // 16 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 256;
+constexpr int kEpiWarps = 8;                   // two per SM sub-partition, each half the columns
+constexpr int kEpiCols = kBN / (kEpiWarps / 4);
+constexpr int kThreads = 32 * (4 + kEpiWarps);
 constexpr uint32_t kTmemCols = 2 * kBN;        // two accumulators of 256 f32 columns
 constexpr int kBarOff = kStages * kStageBytes;
 constexpr int kNumBars = 2 * kStages + 5;      // full, empty, acc full x2, acc empty x2, done
 constexpr int kSmemBytes = kBarOff + 8 * kNumBars + 16 + 1024;   // + slack for 1024-B alignment
 constexpr uint32_t kSpinLimit = 1u << 26;
 
-// Instruction descriptor of the MMA: D in f32 (bits 4-5 = 1), A and B E4M3
-// (bits 7-9 and 10-12 = 0), both K-major (bits 15, 16 = 0), N / 8 in bits
-// 17-22, M / 16 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+// Instruction descriptor of the pair's MMA: D in f32 (bits 4-5 = 1), A and B
+// E4M3 (bits 7-9 and 10-12 = 0), both K-major (bits 15, 16 = 0), N / 8 in
+// bits 17-22, M / 16 in bits 24-28 (M = 256 over the two CTAs).
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)((2 * kBM) >> 4) << 24);
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -84,20 +92,45 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile u
     if (abort) *abort = 1u;
     return false;
 }
+// the common case (the phase has already completed) without the call
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
+    return mbar_try(bar, parity) || mbar_wait(bar, parity, abort);
+}
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+
+// arrive on an mbarrier of either CTA of the cluster (a shared::cluster address)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+
+// ---- clusters ----
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// the shared::cluster address of this CTA's shared address `a` in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+// every thread of both CTAs (the non-.aligned form: lanes of a warp may arrive apart)
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // ---- TMA ----
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                            uint32_t bar) {
+// A 2-D tile into this CTA's shared memory, its bytes counted on `cbar`, an
+// mbarrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 uint32_t cbar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cbar)
         : "memory");
 }
 
@@ -113,19 +146,22 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t accumulate) {
+__device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
         : "memory");
 }
-// arrive on `bar` once every MMA this thread issued before has completed
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+// arrive on the mbarrier at shared address `bar` in every CTA of `mask` once
+// every MMA this thread issued before has completed
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -170,10 +206,14 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
-// One tile's epilogue for this thread's output row: per group of G columns,
-// the maximum of |y|, S, then the codes (and y when asked for).  Columns come
-// from tensor memory in chunks of up to 32; a group wider than a chunk is
-// read twice (maximum, then codes) instead of being held in registers.
+// One tile's epilogue for this thread: one output row, kEpiCols columns from
+// n0.  Per group of G columns: max|acc| (|RN(acc sxw)| is monotone in |acc|,
+// so max|y| = RN(max|acc| sxw)), S = RN(max|y| / 448), then the codes of
+// y = RN(acc sxw) two at a time on the packed f32x2 path: the codes of
+// y inv (1 -+ 2^-20) agree when no E4M3 midpoint lies near y / S, and the
+// rare elements where they differ are decided from the exact quotient.
+// Columns come from tensor memory in chunks of up to 32; a group wider than a
+// chunk is read twice (maximum, then codes) instead of being held in registers.
 template <int G>
 __device__ __forceinline__ void epilogue_row(const LinArgs& a, uint32_t taddr, int64_t row, int64_t n0,
                                              float sxw) {
@@ -181,21 +221,25 @@ __device__ __forceinline__ void epilogue_row(const LinArgs& a, uint32_t taddr, i
     constexpr int kNch = G / kCh;
     const bool row_ok = row < a.M;
     const int64_t ngr = a.N / G;
+    const uint64_t sxw2 = pk(sxw, sxw), zero2 = pk(0.0f, 0.0f), dn2 = pk(kDn, kDn), up2 = pk(kUp, kUp);
 #pragma unroll 1
-    for (int g = 0; g < kBN / G; ++g) {
+    for (int g = 0; g < kEpiCols / G; ++g) {
         const int64_t col0 = n0 + (int64_t)g * G;
         if (col0 >= a.N) break;   // the same for the whole warp
         uint32_t v[kCh];
-        float mx = 0.0f;
+        float mxa = 0.0f;
 #pragma unroll
         for (int c = 0; c < kNch; ++c) {
             __syncwarp();   // tcgen05.ld is warp-collective: converge after the code branches
             tmem_ld<kCh>(taddr + (uint32_t)(g * G + c * kCh), v);
 #pragma unroll
-            for (int e = 0; e < kCh; ++e) mx = fmaxf(mx, fabsf(__fmul_rn(__uint_as_float(v[e]), sxw)));
+            for (int e = 0; e < kCh; e += 2)
+                mxa = max3(mxa, fabsf(__uint_as_float(v[e])), fabsf(__uint_as_float(v[e + 1])));
         }
-        const float S = __fdiv_rn(mx, 448.0f);
+        const float S = __fdiv_rn(__fmul_rn(mxa, sxw), 448.0f);
         const float inv = S > 0.0f ? rcp_approx(S) : 0.0f;
+        const bool inv_bad = !(inv <= 3.40282347e38f);
+        const uint64_t inv2 = pk(inv, inv);
         if (row_ok) a.scale[row * ngr + col0 / G] = S;
 #pragma unroll
         for (int c = 0; c < kNch; ++c) {
@@ -204,18 +248,30 @@ __device__ __forceinline__ void epilogue_row(const LinArgs& a, uint32_t taddr, i
                 tmem_ld<kCh>(taddr + (uint32_t)(g * G + c * kCh), v);
             }
             float y[kCh];
-            uint32_t w[kCh / 4];
+            uint32_t w[kCh / 4], dw[kCh / 4];
 #pragma unroll
-            for (int e = 0; e < kCh; ++e) y[e] = __fmul_rn(__uint_as_float(v[e]), sxw);
+            for (int e = 0; e < kCh; e += 2) {
+                const uint64_t y2 = mul2(pk(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sxw2);
+                upk(y2, y[e], y[e + 1]);
+                const uint64_t yy = fma2(y2, inv2, zero2);   // +0 for a zero of either sign
+                float l0, l1, h0, h1;
+                upk(mul2(yy, dn2), l0, l1);
+                upk(mul2(yy, up2), h0, h1);
+                const uint32_t clo = e4m3x2(l0, l1), chi = e4m3x2(h0, h1);
+                if ((e & 2) == 0) { w[e / 4] = clo; dw[e / 4] = clo ^ chi; }
+                else { w[e / 4] |= clo << 16; dw[e / 4] |= (clo ^ chi) << 16; }
+            }
+            uint32_t any = inv_bad ? 1u : 0u;
 #pragma unroll
-            for (int i = 0; i < kCh / 4; ++i) w[i] = 0u;
-            if (S > 0.0f) {
+            for (int i = 0; i < kCh / 4; ++i) any |= dw[i];
+            if (any != 0u && S > 0.0f) {   // rare: quotients beside a midpoint
 #pragma unroll
                 for (int e = 0; e < kCh; ++e) {
-                    bool und;
-                    uint32_t code = e4m3_code_fast(y[e], inv, und);
-                    if (und) code = e4m3_code_of_quotient_exact(y[e], S);
-                    w[e / 4] |= code << (8 * (e & 3));
+                    const int sh = 8 * (e & 3);
+                    if (inv_bad || ((dw[e / 4] >> sh) & 0xFFu) != 0u) {
+                        const uint32_t code = e4m3_code_of_quotient_exact(y[e], S);
+                        w[e / 4] = (w[e / 4] & ~(0xFFu << sh)) | (code << sh);
+                    }
                 }
             }
             if (row_ok) {
@@ -240,12 +296,28 @@ __device__ __forceinline__ void epilogue_row(const LinArgs& a, uint32_t taddr, i
     }
 }
 
+// Tile order: bands of kGroupM row pairs, column-major inside a band, so the
+// pairs running at once share a band of X (kGroupM x 256 rows, kept in L2)
+// and walk W together, instead of all sweeping X for every column block.
+constexpr int64_t kGroupM = 16;
+struct TileCoord {
+    int64_t m, n;   // row-pair block (256 rows) and column block (256 columns)
+};
+__device__ __forceinline__ TileCoord tile_coord(int64_t t, int64_t num_m, int64_t num_n) {
+    const int64_t band = t / (kGroupM * num_n), first = band * kGroupM;
+    const int64_t rows = num_m - first < kGroupM ? num_m - first : kGroupM;
+    const int64_t r = t - band * kGroupM * num_n;
+    return TileCoord{first + r % rows, r / rows};
+}
+
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_fp8_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                   const LinArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the 128-byte swizzle repeats every 1024 bytes: align the stages to it
+    // (the same offset in both CTAs of the pair: the MMA addresses both rings
+    // with one descriptor)
     const uint32_t raw = smem_u32(smem_raw);
     unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
@@ -259,9 +331,12 @@ linear_fp8_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     volatile uint32_t* abort = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();   // 0: the CTA that issues the pair's MMAs
+    const bool leader = rank == 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(acc_full(b), 1); mbar_init(acc_empty(b), 128); }
+        // the leader's accumulator is free once every epilogue warp of both CTAs is done with it
+        for (int b = 0; b < 2; ++b) { mbar_init(acc_full(b), 1); mbar_init(acc_empty(b), 2 * kEpiWarps); }
         mbar_init(done, 1);
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -269,91 +344,108 @@ linear_fp8_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
     }
     if (warp == 2) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+        // the same columns in both CTAs of the pair
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(kTmemCols)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();   // barriers initialised and tensor memory allocated in both CTAs
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int64_t num_m = (a.M + kBM - 1) / kBM, num_n = (a.N + kBN - 1) / kBN;
+    const int64_t num_m = (a.M + 2 * kBM - 1) / (2 * kBM), num_n = (a.N + kBN - 1) / kBN;
     const int64_t tiles = num_m * num_n;
     const int kblocks = (int)((a.K + kBK - 1) / kBK);
+    const int64_t cid = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
     if (warp == 0 && lane == 0) {
-        // ---- TMA producer ----
+        // ---- TMA producer (both CTAs): this CTA's rows of X and of W ----
         int s = 0;
         uint32_t ph = 0, issued = 0, last_ph = 0;   // per stage: issued at all, parity of the last issue
         bool ok = true;
-        for (int64_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-            const int32_t m0 = (int32_t)((t % num_m) * kBM), n0 = (int32_t)((t / num_m) * kBN);
+        const uint32_t fb0 = map_to_rank(full(0), 0);   // the leader's barriers, contiguous like ours
+        for (int64_t t = cid; ok && t < tiles; t += nclusters) {
+            const TileCoord tc = tile_coord(t, num_m, num_n);
+            const int32_t m0 = (int32_t)(tc.m * (2 * kBM) + rank * kBM);
+            const int32_t n0 = (int32_t)(tc.n * kBN + rank * kBNh);
             for (int kb = 0; kb < kblocks; ++kb) {
-                if (!mbar_wait(empty(s), ph ^ 1u, abort)) { ok = false; break; }
-                mbar_expect_tx(full(s), (uint32_t)kStageBytes);
+                if (!mbar_wait_fast(empty(s), ph ^ 1u, abort)) { ok = false; break; }
+                // the leader's barrier counts the bytes of both CTAs
+                if (leader) mbar_expect_tx(full(s), (uint32_t)(2 * kStageBytes));
+                const uint32_t fb = fb0 + 8u * (uint32_t)s;
                 const uint32_t sa = sb + (uint32_t)(s * kStageBytes);
-                tma_load_2d(sa, &tmx, kb * kBK, m0, full(s));
-                tma_load_2d(sa + kABytes, &tmw, kb * kBK, n0, full(s));
+                tma_load_2d_pair(sa, &tmx, kb * kBK, m0, fb);
+                tma_load_2d_pair(sa + kABytes, &tmw, kb * kBK, n0, fb);
                 issued |= 1u << s;
                 last_ph = (last_ph & ~(1u << s)) | (ph << s);
                 if (++s == kStages) { s = 0; ph ^= 1u; }
             }
         }
-        // every copy issued has landed before the CTA may exit
+        // every stage issued has been read by the MMAs (and the release that
+        // says so has landed here) before the CTA may exit
         for (int i = 0; i < kStages; ++i)
-            if (issued & (1u << i)) mbar_wait(full(i), (last_ph >> i) & 1u, nullptr);
+            if (issued & (1u << i)) mbar_wait(empty(i), (last_ph >> i) & 1u, nullptr);
     } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer ----
-        int s = 0, acc = 0;
-        uint32_t ph = 0, aph = 0;
-        bool ok = true;
-        for (int64_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-            if (!mbar_wait(acc_empty(acc), aph ^ 1u, abort)) break;
-            tc_fence_after();
-            const uint32_t d = tmem + (uint32_t)(acc * kBN);
-            for (int kb = 0; kb < kblocks; ++kb) {
-                if (!mbar_wait(full(s), ph, abort)) { ok = false; break; }
+        if (leader) {
+            // ---- MMA issuer (even CTA) ----
+            int s = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            // descriptors of stage 0; a stage / K step moves only the start
+            // address field (address / 16, 14 bits, no carry out for shared addresses)
+            const uint64_t adesc0 = sw128_desc(sb), bdesc0 = sw128_desc(sb + kABytes);
+            for (int64_t t = cid; ok && t < tiles; t += nclusters) {
+                if (!mbar_wait_fast(acc_empty(acc), aph ^ 1u, abort)) break;
                 tc_fence_after();
-                const uint32_t sa = sb + (uint32_t)(s * kStageBytes), sbb = sa + kABytes;
+                const uint32_t d = tmem + (uint32_t)(acc * kBN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_fast(full(s), ph, abort)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t so = (uint64_t)(s * (kStageBytes >> 4));
 #pragma unroll
-                for (int kk = 0; kk < kBK / kMmaK; ++kk)
-                    mma_e4m3(d, sw128_desc(sa + kk * kMmaK), sw128_desc(sbb + kk * kMmaK), (kb | kk) != 0);
-                mma_commit(empty(s));   // the stage is free once these MMAs have read it
-                if (++s == kStages) { s = 0; ph ^= 1u; }
+                    for (int kk = 0; kk < kBK / kMmaK; ++kk)
+                        mma_e4m3_pair(d, adesc0 + so + (uint64_t)(kk * (kMmaK >> 4)),
+                                      bdesc0 + so + (uint64_t)(kk * (kMmaK >> 4)), (kb | kk) != 0);
+                    mma_commit_pair(empty(s), 0x3);   // both CTAs' stage s is free once read
+                    if (++s == kStages) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit_pair(acc_full(acc), 0x3);
+                acc ^= 1;
+                if (acc == 0) aph ^= 1u;
             }
-            if (!ok) break;
-            mma_commit(acc_full(acc));
-            acc ^= 1;
-            if (acc == 0) aph ^= 1u;
+            // every MMA issued has completed before either CTA frees tensor memory
+            mma_commit_pair(done, 0x3);
         }
-        // every MMA issued has completed before tensor memory is freed
-        mma_commit(done);
         mbar_wait(done, 0u, nullptr);
     } else if (warp >= 4) {
-        // ---- epilogue: warp 4 + i reads tensor-memory lanes 32 i .. 32 i + 31 ----
-        const int q4 = warp & 3;
+        // ---- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. 32 (w % 4) + 31
+        // (the sub-partition it runs on), columns kEpiCols (w - 4) / 4 onwards ----
+        const int q4 = warp & 3, ch = (warp - 4) >> 2;
         const float sxw = __fmul_rn(a.sx, a.sw);
         int acc = 0;
         uint32_t aph = 0;
-        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-            if (!mbar_wait(acc_full(acc), aph, abort)) break;
+        for (int64_t t = cid; t < tiles; t += nclusters) {
+            if (!mbar_wait_fast(acc_full(acc), aph, abort)) break;
             tc_fence_after();
-            const int64_t row = (t % num_m) * kBM + 32 * q4 + lane;
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(acc * kBN);
-            epilogue_row<G>(a, taddr, row, (t / num_m) * kBN, sxw);
+            const TileCoord tc = tile_coord(t, num_m, num_n);
+            const int64_t row = tc.m * (2 * kBM) + rank * kBM + 32 * q4 + lane;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(acc * kBN + ch * kEpiCols);
+            epilogue_row<G>(a, taddr, row, tc.n * kBN + ch * kEpiCols, sxw);
             tc_fence_before();
-            mbar_arrive(acc_empty(acc));
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(acc_empty(acc), 0));
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
         }
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();   // no arrival or copy is still on its way to either CTA
     tc_fence_after();
     if (warp == 2)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
 }
 
@@ -392,17 +484,30 @@ bool encode_operand(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t
 template <int G>
 cudaError_t launch_linear_g(const LinArgs& a, cudaStream_t s) {
     alignas(64) CUtensorMap tmx, tmw;
-    if (!encode_operand(&tmx, a.xq, a.M, a.K, kBM) || !encode_operand(&tmw, a.wq, a.N, a.K, kBN))
+    if (!encode_operand(&tmx, a.xq, a.M, a.K, kBM) || !encode_operand(&tmw, a.wq, a.N, a.K, kBNh))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(linear_fp8_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
-    const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
-    linear_fp8_kernel<G><<<grid, kThreads, kSmemBytes, s>>>(tmx, tmw, a);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2);
+    int clusters = 0;   // CTA pairs that fit on the GPU at once
+    if ((e = cudaOccupancyMaxActiveClusters(&clusters, linear_fp8_kernel<G>, &cfg)) != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    const int64_t tiles = ((a.M + 2 * kBM - 1) / (2 * kBM)) * ((a.N + kBN - 1) / kBN);
+    cfg.gridDim = dim3(2u * (unsigned)(tiles < clusters ? tiles : clusters));
+    e = cudaLaunchKernelEx(&cfg, linear_fp8_kernel<G>, tmx, tmw, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -6,9 +6,10 @@ COAT review page, section 3: linear layers take per-tensor FP8 inputs
 quantizes its output tile per 1 x G group ("Triton kernels", linear layer
 optimisation).
 
-The kernel runs on the fifth-generation tensor cores (TMA-fed shared-memory
-ring, accumulators in tensor memory) and accumulates in float32, so its y is not the
-oracle's correctly rounded one; the checks are
+The kernel runs on the fifth-generation tensor cores (CTA pairs sharing one
+MMA, TMA-fed shared-memory rings, accumulators in tensor memory) and
+accumulates in float32, so its y is not the oracle's correctly rounded one;
+the checks are
   * y within the float32 summation bound (K + 2) 2^-24 |sx sw| sum_k |x_k w_k|
     of the oracle's y (K - 1 additions, the product by RN(sx sw) and that
     rounding itself, each at most half an ulp of a partial sum);
@@ -102,9 +103,9 @@ def test_ragged_shapes(M, N, K, G):
 
 
 def test_more_tiles_than_sms():
-    """320 tiles: each persistent CTA takes two or three, alternating between
-    its two tensor-memory accumulators."""
-    M, N, K, G = 128 * 40, 256 * 8, 256, 32
+    """160 tiles of 256 x 256: each persistent CTA pair takes two or more,
+    alternating between its two tensor-memory accumulators."""
+    M, N, K, G = 256 * 20, 256 * 8, 256, 32
     xq = synth.fp8_operand_codes_np(M, K, 31)
     wq = synth.fp8_operand_codes_np(N, K, 32)
     y, q, S = _gpu(xq, 0.031, wq, 0.0047, G)
