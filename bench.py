@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "FP8 AdamW+DRE step: params/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL = "step_kernel_cta"
 L2_BYTES = 129 * 2 ** 20
 
@@ -49,12 +50,18 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
-    p.add_argument("--report", default=None, choices=["dre-mse", "act-quant", "g-sweep"],
+    p.add_argument("--report", default=None, choices=["dre-mse", "act-quant", "g-sweep", "linear"],
                    help="dre-mse: quantization error with and without the expansion on "
                         "AdamW-like moments, and the codec kernels' bandwidth; act-quant: "
                         "bandwidth of the per-group FP8 activation quantizer (one GPU); "
                         "g-sweep: the step over --sweep-workload for G in --sweep-G, one "
-                        "JSON line per G with its roofline and clocks")
+                        "JSON line per G with its roofline and clocks; linear: the FP8 linear "
+                        "layer with per-group FP8 output on Llama-2-7B layer shapes, one JSON "
+                        "line per shape against the tensor-core roofline")
+    p.add_argument("--lin-tokens", type=int, default=8192, help="M (tokens) of the linear report")
+    p.add_argument("--lin-G", type=int, default=16, help="output group size of the linear report")
+    p.add_argument("--lin-shapes", default="attn_qkvo,mlp_up_gate,mlp_down,square_16k_8k_8k",
+                   help="layers of the linear report (comma-separated)")
     p.add_argument("--sweep-workload", default="llama13b")
     p.add_argument("--sweep-G", default="16,32,64,128,256")
     p.add_argument("--rows", type=int, default=32768, help="M of the act-quant report")
@@ -601,6 +608,105 @@ def report_act_quant(args):
     print(json.dumps(out), flush=True)
 
 
+def measured_fp8_peak():
+    """Dense FP8 tensor peak: the measured bf16 GEMM burst rate times the
+    nominal FP8:bf16 ratio of 2 (4.5 / 2.25 PFLOP/s dense)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return 2.0 * float(d["bf16_tflops"]), "measured bf16 burst x 2 (nominal fp8:bf16)"
+    except (OSError, KeyError, ValueError):
+        return 2.0 * FALLBACK_BF16_TFLOPS, "fallback bf16 x 2 (nominal fp8:bf16)"
+
+
+def report_linear(args):
+    """The FP8 linear layer with a per-group FP8 output (coat_fp8_linear_group_quantize)
+    on the linear layers of a Llama-2-7B block over --lin-tokens tokens (q/k/v/o,
+    MLP up/gate, MLP down) and one 16384 x 8192 x 8192 product: CUDA events per
+    batch of launches on the launching stream, clocks sampled meanwhile, against
+    the dense FP8 tensor roofline.  A plain FP8 GEMM from the library
+    (torch._scaled_mm, bf16 output, no group quantization) is timed beside it
+    for context."""
+    import torch
+
+    import coat_fp8_adamw_gb300 as coat
+    from coat_fp8_adamw_gb300 import synth
+    coat.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    T, G = args.lin_tokens, args.lin_G
+    peak, peak_kind = measured_fp8_peak()
+    stream = torch.cuda.current_stream(dev)
+    shapes = [("attn_qkvo", T, 4096, 4096), ("mlp_up_gate", T, 11008, 4096),
+              ("mlp_down", T, 4096, 11008), ("square_16k_8k_8k", 16384, 8192, 8192)]
+    wanted = set(args.lin_shapes.split(","))
+    for name, M, N, K in shapes:
+        if name not in wanted:
+            continue
+        xq = torch.from_numpy(synth.fp8_operand_codes_np(M, K, 1)).to(dev)
+        wq = torch.from_numpy(synth.fp8_operand_codes_np(N, K, 2)).to(dev)
+        q = torch.empty((M, N), dtype=torch.uint8, device=dev)
+        S = torch.empty((M, N // G), dtype=torch.float32, device=dev)
+        sx, sw = 0.02, 0.003
+
+        def run():
+            coat.coat_fp8_linear_group_quantize(xq, sx, wq, sw, G, q, S, stream=stream)
+
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        coat.coat_kernel_wait_timeouts(reset=True)
+        # enough launches for half a second of clock samples
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        for _ in range(5):
+            run()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        reps = max(20, int(500.0 / max(ev[0].elapsed_time(ev[1]) / 5, 1e-3)))
+        clocks = ClockSampler(0)
+        clocks.start()
+        ev[0].record(stream)
+        for _ in range(reps):
+            run()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+        ms = ev[0].elapsed_time(ev[1]) / reps
+        timeouts = coat.coat_kernel_wait_timeouts(reset=True)
+        flops = 2.0 * M * N * K
+        tf = flops / (ms / 1e3) / 1e12
+        lib_ms = None
+        try:
+            a8, b8 = xq.view(torch.float8_e4m3fn), wq.view(torch.float8_e4m3fn)
+            one = torch.ones((), device=dev)
+            for _ in range(3):
+                torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            torch.cuda.synchronize()
+            ev[0].record(stream)
+            for _ in range(20):
+                torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            lib_ms = ev[0].elapsed_time(ev[1]) / 20
+        except (RuntimeError, AttributeError, TypeError):
+            pass
+        print(json.dumps({
+            "report": "linear", "layer": name, "M": M, "N": N, "K": K, "G": G,
+            "metric": "fp8_linear_group_quantize_tflops", "value": tf, "unit": "TFLOP/s",
+            "ms": ms, "launches_timed": reps, "data": "synthetic E4M3 codes (activation-like magnitudes)",
+            "dtype": "e4m3 x e4m3 -> f32 accumulate -> e4m3 codes + f32 group scales",
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak, "peak_kind": peak_kind,
+                         "traffic": None, "kernel": "linear_fp8_kernel"},
+            "output_bytes": M * N + 4 * (M * N // G),
+            "library_fp8_gemm": None if lib_ms is None else {
+                "what": "torch._scaled_mm, bf16 output, no group quantization",
+                "ms": lib_ms, "tflops": flops / (lib_ms / 1e3) / 1e12},
+            "wait_timeouts": timeouts, "clocks": clk}), flush=True)
+
+
 def report_g_sweep(args):
     """The step over one model-shaped parameter set for several group sizes
     (the 13B configuration sweeps G = 16 ... 256): weights and three cycled
@@ -677,6 +783,9 @@ def main():
     args = parse()
     if args.report == "g-sweep":
         report_g_sweep(args)
+        return
+    if args.report == "linear":
+        report_linear(args)
         return
     if args.report == "dre-mse":
         report_dre_mse(args)

@@ -167,29 +167,9 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // 32 lanes x N consecutive 32-bit columns: thread i receives lane (taddr's lane + i)
+// (the wait for the registers is part of the same statement)
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]);
-template <>
-__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, uint32_t (&r)[8]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-        : "r"(taddr)
-        : "memory");
-}
-template <>
-__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-        "%12, %13, %14, %15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-}
 template <>
 __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -206,91 +186,153 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// Codes of 2 n values of one row, y = RN(acc sxw), on the packed f32x2 path:
+// the codes of y inv (1 -+ 2^-20) agree when no E4M3 midpoint lies near
+// y / S, and the rare elements where they differ (or where the reciprocal is
+// not finite) are decided from the exact quotient.  inv[e / kPer] and
+// S[e / kPer] belong to element e.
+template <int n, int kPer>
+__device__ __forceinline__ void codes_of(const uint32_t* v, float sxw, const float* S, const float* inv,
+                                         float* y, uint32_t* w) {
+    const uint64_t sxw2 = pk(sxw, sxw), zero2 = pk(0.0f, 0.0f), dn2 = pk(kDn, kDn), up2 = pk(kUp, kUp);
+    uint32_t dw[n / 4];
+#pragma unroll
+    for (int e = 0; e < n; e += 2) {
+        const uint64_t y2 = mul2(pk(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sxw2);
+        upk(y2, y[e], y[e + 1]);
+        const uint64_t yy = fma2(y2, pk(inv[e / kPer], inv[(e + 1) / kPer]), zero2);   // +0 for -0
+        float l0, l1, h0, h1;
+        upk(mul2(yy, dn2), l0, l1);
+        upk(mul2(yy, up2), h0, h1);
+        const uint32_t clo = e4m3x2(l0, l1), chi = e4m3x2(h0, h1);
+        if ((e & 2) == 0) { w[e / 4] = clo; dw[e / 4] = clo ^ chi; }
+        else { w[e / 4] |= clo << 16; dw[e / 4] |= (clo ^ chi) << 16; }
+    }
+    uint32_t any = 0u;
+#pragma unroll
+    for (int i = 0; i < n / 4; ++i) any |= dw[i];
+#pragma unroll
+    for (int j = 0; j < (n + kPer - 1) / kPer; ++j) any |= (inv[j] <= 3.40282347e38f) ? 0u : 1u;
+    if (any != 0u) {   // rare: quotients beside a midpoint
+#pragma unroll
+        for (int e = 0; e < n; ++e) {
+            const int sh = 8 * (e & 3);
+            const bool bad = !(inv[e / kPer] <= 3.40282347e38f);
+            if (S[e / kPer] > 0.0f && (bad || ((dw[e / 4] >> sh) & 0xFFu) != 0u)) {
+                const uint32_t code = e4m3_code_of_quotient_exact(y[e], S[e / kPer]);
+                w[e / 4] = (w[e / 4] & ~(0xFFu << sh)) | (code << sh);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < n / 4; ++i) w[i] = e4m3_canonical_zero(w[i]);
+}
+
+// the codes (and y when asked for) of n columns from col of this thread's row
+template <int n>
+__device__ __forceinline__ void store_codes(const LinArgs& a, int64_t row, int64_t col, const uint32_t* w,
+                                            const float* y) {
+    uint8_t* qp = a.q + row * a.N + col;
+    if constexpr (n == 8) {
+        *reinterpret_cast<uint2*>(qp) = make_uint2(w[0], w[1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < n / 16; ++i)
+            reinterpret_cast<uint4*>(qp)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+    if (a.y) {
+        float4* yp = reinterpret_cast<float4*>(a.y + row * a.N + col);
+#pragma unroll
+        for (int i = 0; i < n / 4; ++i) yp[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+    }
+}
+
 // One tile's epilogue for this thread: one output row, kEpiCols columns from
 // n0.  Per group of G columns: max|acc| (|RN(acc sxw)| is monotone in |acc|,
-// so max|y| = RN(max|acc| sxw)), S = RN(max|y| / 448), then the codes of
-// y = RN(acc sxw) two at a time on the packed f32x2 path: the codes of
-// y inv (1 -+ 2^-20) agree when no E4M3 midpoint lies near y / S, and the
-// rare elements where they differ are decided from the exact quotient.
-// Columns come from tensor memory in chunks of up to 32; a group wider than a
-// chunk is read twice (maximum, then codes) instead of being held in registers.
+// so max|y| = RN(max|acc| sxw)), S = RN(max|y| / 448), then the codes.
+// Columns come from tensor memory 32 at a time: a chunk holds 32 / G whole
+// groups when G <= 32, and a wider group is read twice (maximum, then codes)
+// instead of being held in registers.
 template <int G>
 __device__ __forceinline__ void epilogue_row(const LinArgs& a, uint32_t taddr, int64_t row, int64_t n0,
                                              float sxw) {
-    constexpr int kCh = G < 32 ? G : 32;
-    constexpr int kNch = G / kCh;
+    constexpr int kCh = 32;
     const bool row_ok = row < a.M;
     const int64_t ngr = a.N / G;
-    const uint64_t sxw2 = pk(sxw, sxw), zero2 = pk(0.0f, 0.0f), dn2 = pk(kDn, kDn), up2 = pk(kUp, kUp);
+    if constexpr (G <= kCh) {
+        constexpr int kGpc = kCh / G;
 #pragma unroll 1
-    for (int g = 0; g < kEpiCols / G; ++g) {
-        const int64_t col0 = n0 + (int64_t)g * G;
-        if (col0 >= a.N) break;   // the same for the whole warp
-        uint32_t v[kCh];
-        float mxa = 0.0f;
-#pragma unroll
-        for (int c = 0; c < kNch; ++c) {
+        for (int c = 0; c < kEpiCols / kCh; ++c) {
+            const int64_t col0 = n0 + (int64_t)c * kCh;
+            if (col0 >= a.N) break;   // the same for the whole warp
+            uint32_t v[kCh];
             __syncwarp();   // tcgen05.ld is warp-collective: converge after the code branches
-            tmem_ld<kCh>(taddr + (uint32_t)(g * G + c * kCh), v);
+            tmem_ld<kCh>(taddr + (uint32_t)(c * kCh), v);
+            float S[kGpc], inv[kGpc];
 #pragma unroll
-            for (int e = 0; e < kCh; e += 2)
-                mxa = max3(mxa, fabsf(__uint_as_float(v[e])), fabsf(__uint_as_float(v[e + 1])));
-        }
-        const float S = __fdiv_rn(__fmul_rn(mxa, sxw), 448.0f);
-        const float inv = S > 0.0f ? rcp_approx(S) : 0.0f;
-        const bool inv_bad = !(inv <= 3.40282347e38f);
-        const uint64_t inv2 = pk(inv, inv);
-        if (row_ok) a.scale[row * ngr + col0 / G] = S;
+            for (int j = 0; j < kGpc; ++j) {
+                float mxa = 0.0f;
 #pragma unroll
-        for (int c = 0; c < kNch; ++c) {
-            if (kNch > 1) {
-                __syncwarp();
-                tmem_ld<kCh>(taddr + (uint32_t)(g * G + c * kCh), v);
+                for (int e = j * G; e < (j + 1) * G; e += 2)
+                    mxa = max3(mxa, fabsf(__uint_as_float(v[e])), fabsf(__uint_as_float(v[e + 1])));
+                S[j] = __fdiv_rn(__fmul_rn(mxa, sxw), 448.0f);
+                inv[j] = S[j] > 0.0f ? rcp_approx(S[j]) : 0.0f;
             }
             float y[kCh];
-            uint32_t w[kCh / 4], dw[kCh / 4];
+            uint32_t w[kCh / 4];
+            codes_of<kCh, G>(v, sxw, S, inv, y, w);
+            if (row_ok) {
+                const int64_t si = row * ngr + col0 / G;
+                if (col0 + kCh <= a.N) {   // the whole chunk: one store of codes, scales together
+                    store_codes<kCh>(a, row, col0, w, y);
+                    if constexpr (kGpc == 4) {
+                        if ((si & 3) == 0) *reinterpret_cast<float4*>(a.scale + si) = make_float4(S[0], S[1], S[2], S[3]);
+                        else for (int j = 0; j < 4; ++j) a.scale[si + j] = S[j];
+                    } else if constexpr (kGpc == 2) {
+                        if ((si & 1) == 0) *reinterpret_cast<float2*>(a.scale + si) = make_float2(S[0], S[1]);
+                        else for (int j = 0; j < 2; ++j) a.scale[si + j] = S[j];
+                    } else {
+                        a.scale[si] = S[0];
+                    }
+                } else {   // N is a multiple of G, not of the chunk
 #pragma unroll
-            for (int e = 0; e < kCh; e += 2) {
-                const uint64_t y2 = mul2(pk(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sxw2);
-                upk(y2, y[e], y[e + 1]);
-                const uint64_t yy = fma2(y2, inv2, zero2);   // +0 for a zero of either sign
-                float l0, l1, h0, h1;
-                upk(mul2(yy, dn2), l0, l1);
-                upk(mul2(yy, up2), h0, h1);
-                const uint32_t clo = e4m3x2(l0, l1), chi = e4m3x2(h0, h1);
-                if ((e & 2) == 0) { w[e / 4] = clo; dw[e / 4] = clo ^ chi; }
-                else { w[e / 4] |= clo << 16; dw[e / 4] |= (clo ^ chi) << 16; }
-            }
-            uint32_t any = inv_bad ? 1u : 0u;
-#pragma unroll
-            for (int i = 0; i < kCh / 4; ++i) any |= dw[i];
-            if (any != 0u && S > 0.0f) {   // rare: quotients beside a midpoint
-#pragma unroll
-                for (int e = 0; e < kCh; ++e) {
-                    const int sh = 8 * (e & 3);
-                    if (inv_bad || ((dw[e / 4] >> sh) & 0xFFu) != 0u) {
-                        const uint32_t code = e4m3_code_of_quotient_exact(y[e], S);
-                        w[e / 4] = (w[e / 4] & ~(0xFFu << sh)) | (code << sh);
+                    for (int j = 0; j < kGpc; ++j) {
+                        const int64_t col = col0 + j * G;
+                        if (col < a.N) {
+                            a.scale[si + j] = S[j];
+                            store_codes<G>(a, row, col, w + j * (G / 4), y + j * G);
+                        }
                     }
                 }
             }
-            if (row_ok) {
-                uint8_t* qp = a.q + row * a.N + col0 + c * kCh;
-                if constexpr (kCh == 8) {
-                    *reinterpret_cast<uint2*>(qp) = make_uint2(e4m3_canonical_zero(w[0]), e4m3_canonical_zero(w[1]));
-                } else {
+        }
+    } else {
+        constexpr int kNch = G / kCh;
+#pragma unroll 1
+        for (int g = 0; g < kEpiCols / G; ++g) {
+            const int64_t col0 = n0 + (int64_t)g * G;
+            if (col0 >= a.N) break;
+            uint32_t v[kCh];
+            float mxa = 0.0f;
 #pragma unroll
-                    for (int i = 0; i < kCh / 16; ++i)
-                        reinterpret_cast<uint4*>(qp)[i] =
-                            make_uint4(e4m3_canonical_zero(w[4 * i]), e4m3_canonical_zero(w[4 * i + 1]),
-                                       e4m3_canonical_zero(w[4 * i + 2]), e4m3_canonical_zero(w[4 * i + 3]));
-                }
-                if (a.y) {
-                    float4* yp = reinterpret_cast<float4*>(a.y + row * a.N + col0 + c * kCh);
+            for (int c = 0; c < kNch; ++c) {
+                __syncwarp();
+                tmem_ld<kCh>(taddr + (uint32_t)(g * G + c * kCh), v);
 #pragma unroll
-                    for (int i = 0; i < kCh / 4; ++i)
-                        yp[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
-                }
+                for (int e = 0; e < kCh; e += 2)
+                    mxa = max3(mxa, fabsf(__uint_as_float(v[e])), fabsf(__uint_as_float(v[e + 1])));
+            }
+            const float S = __fdiv_rn(__fmul_rn(mxa, sxw), 448.0f);
+            const float inv = S > 0.0f ? rcp_approx(S) : 0.0f;
+            if (row_ok) a.scale[row * ngr + col0 / G] = S;
+#pragma unroll
+            for (int c = 0; c < kNch; ++c) {
+                __syncwarp();
+                tmem_ld<kCh>(taddr + (uint32_t)(g * G + c * kCh), v);
+                float y[kCh];
+                uint32_t w[kCh / 4];
+                codes_of<kCh, kCh>(v, sxw, &S, &inv, y, w);
+                if (row_ok) store_codes<kCh>(a, row, col0 + c * kCh, w, y);
             }
         }
     }
