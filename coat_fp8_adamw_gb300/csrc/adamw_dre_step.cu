@@ -320,13 +320,38 @@ __device__ __forceinline__ void fast_elem(const StepArgs& a, uint32_t wm, uint32
     w = fmaf(mt, rcp_ftz(fmaf(sqrt_ftz(vt), a.sq, a.ep)), __fmul_rn(w, a.decay));
 }
 
+// Elements I and I + 1 of a packed word on the packed f32x2 path: every
+// product and FMA is the scalar one of fast_elem, two lanes per instruction.
+template <int I>
+__device__ __forceinline__ void fast_pair(const StepArgs& a, uint32_t wm, uint32_t wv, float g0, float g1,
+                                          float& w0, float& w1, const float* lg, float bPm, float rkm,
+                                          float bPv, float rkv, float& m0, float& m1, float& v0, float& v1) {
+    float pm0, pm1, pv0, pv1;
+    upk(mul2(pk(table_at(lg, code_off<I>(wm)), table_at(lg, code_off<I + 1>(wm))), pk(rkm, rkm)), pm0, pm1);
+    upk(mul2(pk(table_at(lg, code_off<I>(wv)), table_at(lg, code_off<I + 1>(wv))), pk(rkv, rkv)), pv0, pv1);
+    const float bPs0 = __uint_as_float(__float_as_uint(bPm) ^ ((wm << (24 - 8 * I)) & 0x80000000u));
+    const float bPs1 = __uint_as_float(__float_as_uint(bPm) ^ ((wm << (16 - 8 * I)) & 0x80000000u));
+    const uint64_t gg = pk(g0, g1);
+    const uint64_t mt = fma2(pk(bPs0, bPs1), pk(ex2_ftz(pm0), ex2_ftz(pm1)), fma2(pk(a.omb1, a.omb1), gg, pk(0.0f, 0.0f)));
+    const uint64_t vt = fma2(pk(bPv, bPv), pk(ex2_ftz(pv0), ex2_ftz(pv1)), mul2(mul2(pk(a.omb2, a.omb2), gg), gg));
+    upk(mt, m0, m1);
+    upk(vt, v0, v1);
+    float d0, d1;
+    upk(fma2(pk(sqrt_ftz(v0), sqrt_ftz(v1)), pk(a.sq, a.sq), pk(a.ep, a.ep)), d0, d1);
+    upk(fma2(mt, pk(rcp_ftz(d0), rcp_ftz(d1)), mul2(pk(w0, w1), pk(a.decay, a.decay))), w0, w1);
+}
+
 __device__ __forceinline__ uint32_t encode_pair_m(float m0, float m1, float k, float inv, float cz) {
-    const float y0 = copysignf(ex2_ftz(fmaf(k, lg2_ftz(fabsf(m0) * inv), cz)), m0);
-    const float y1 = copysignf(ex2_ftz(fmaf(k, lg2_ftz(fabsf(m1) * inv), cz)), m1);
-    return e4m3x2(y0, y1);
+    float a0, a1, b0, b1;
+    upk(mul2(pk(fabsf(m0), fabsf(m1)), pk(inv, inv)), a0, a1);
+    upk(fma2(pk(k, k), pk(lg2_ftz(a0), lg2_ftz(a1)), pk(cz, cz)), b0, b1);
+    return e4m3x2(copysignf(ex2_ftz(b0), m0), copysignf(ex2_ftz(b1), m1));
 }
 __device__ __forceinline__ uint32_t encode_pair_v(float v0, float v1, float k, float inv, float cz) {
-    return e4m3x2(ex2_ftz(fmaf(k, lg2_ftz(v0 * inv), cz)), ex2_ftz(fmaf(k, lg2_ftz(v1 * inv), cz)));
+    float a0, a1, b0, b1;
+    upk(mul2(pk(v0, v1), pk(inv, inv)), a0, a1);
+    upk(fma2(pk(k, k), pk(lg2_ftz(a0), lg2_ftz(a1)), pk(cz, cz)), b0, b1);
+    return e4m3x2(ex2_ftz(b0), ex2_ftz(b1));
 }
 
 // ---------------------------------------------------------------------------
@@ -521,10 +546,10 @@ step_kernel_cta(const StepArgs a) {
             float mt[4], vt[4];
             const float g0 = bf16_of(c.g, 4 * q), g1 = bf16_of(c.g, 4 * q + 1);
             const float g2 = bf16_of(c.g, 4 * q + 2), g3 = bf16_of(c.g, 4 * q + 3);
-            fast_elem<0>(a, c.mq[q], c.vq[q], g0, c.w[4 * q], lg_hi, bPm, rkm, bPv, rkv, mt[0], vt[0]);
-            fast_elem<1>(a, c.mq[q], c.vq[q], g1, c.w[4 * q + 1], lg_hi, bPm, rkm, bPv, rkv, mt[1], vt[1]);
-            fast_elem<2>(a, c.mq[q], c.vq[q], g2, c.w[4 * q + 2], lg_hi, bPm, rkm, bPv, rkv, mt[2], vt[2]);
-            fast_elem<3>(a, c.mq[q], c.vq[q], g3, c.w[4 * q + 3], lg_hi, bPm, rkm, bPv, rkv, mt[3], vt[3]);
+            fast_pair<0>(a, c.mq[q], c.vq[q], g0, g1, c.w[4 * q], c.w[4 * q + 1], lg_hi, bPm, rkm, bPv, rkv,
+                         mt[0], mt[1], vt[0], vt[1]);
+            fast_pair<2>(a, c.mq[q], c.vq[q], g2, g3, c.w[4 * q + 2], c.w[4 * q + 3], lg_hi, bPm, rkm, bPv,
+                         rkv, mt[2], mt[3], vt[2], vt[3]);
             lmx_g = fmax3(fmax3(lmx_g, fabsf(g0), fabsf(g1)), fabsf(g2), fabsf(g3));
             lmx_m = fmax3(fmax3(lmx_m, fabsf(mt[0]), fabsf(mt[1])), fabsf(mt[2]), fabsf(mt[3]));
             lmx_v = fmax3(fmax3(lmx_v, vt[0], vt[1]), vt[2], vt[3]);
