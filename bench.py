@@ -608,26 +608,29 @@ def report_act_quant(args):
     print(json.dumps(out), flush=True)
 
 
-def measured_fp8_peak():
-    """Dense FP8 tensor peak: the measured bf16 GEMM burst rate times the
-    nominal FP8:bf16 ratio of 2 (4.5 / 2.25 PFLOP/s dense)."""
+def measured_fp8_peaks():
+    """Dense FP8 tensor peaks (burst, sustained): the measured bf16 GEMM rates
+    times the nominal FP8:bf16 ratio of 2 (4.5 / 2.25 PFLOP/s dense)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(p) as fh:
             d = json.load(fh)
-        return 2.0 * float(d["bf16_tflops"]), "measured bf16 burst x 2 (nominal fp8:bf16)"
+        burst = 2.0 * float(d["bf16_tflops"])
+        sust = 2.0 * float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))
+        return burst, sust, "measured bf16 x 2 (nominal fp8:bf16)"
     except (OSError, KeyError, ValueError):
-        return 2.0 * FALLBACK_BF16_TFLOPS, "fallback bf16 x 2 (nominal fp8:bf16)"
+        return 2.0 * FALLBACK_BF16_TFLOPS, 2.0 * FALLBACK_BF16_TFLOPS, "fallback bf16 x 2"
 
 
 def report_linear(args):
     """The FP8 linear layer with a per-group FP8 output (coat_fp8_linear_group_quantize)
     on the linear layers of a Llama-2-7B block over --lin-tokens tokens (q/k/v/o,
-    MLP up/gate, MLP down) and one 16384 x 8192 x 8192 product: CUDA events per
-    batch of launches on the launching stream, clocks sampled meanwhile, against
-    the dense FP8 tensor roofline.  A plain FP8 GEMM from the library
-    (torch._scaled_mm, bf16 output, no group quantization) is timed beside it
-    for context."""
+    MLP up/gate, MLP down) and one 16384 x 8192 x 8192 product, one JSON line per
+    shape.  Burst: 20 back-to-back launches (CUDA events on the launching
+    stream) against the burst FP8 peak, with a plain FP8 GEMM from the library
+    (torch._scaled_mm, bf16 output, no group quantization) timed the same way
+    just before for context.  Sustained: launches for half a second with the
+    clocks sampled, against the sustained (power-capped) peak."""
     import torch
 
     import coat_fp8_adamw_gb300 as coat
@@ -636,11 +639,21 @@ def report_linear(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     T, G = args.lin_tokens, args.lin_G
-    peak, peak_kind = measured_fp8_peak()
+    peak_b, peak_s, peak_kind = measured_fp8_peaks()
     stream = torch.cuda.current_stream(dev)
     shapes = [("attn_qkvo", T, 4096, 4096), ("mlp_up_gate", T, 11008, 4096),
               ("mlp_down", T, 4096, 11008), ("square_16k_8k_8k", 16384, 8192, 8192)]
     wanted = set(args.lin_shapes.split(","))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed(fn, reps):
+        ev[0].record(stream)
+        for _ in range(reps):
+            fn()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / reps
+
     for name, M, N, K in shapes:
         if name not in wanted:
             continue
@@ -649,62 +662,48 @@ def report_linear(args):
         q = torch.empty((M, N), dtype=torch.uint8, device=dev)
         S = torch.empty((M, N // G), dtype=torch.float32, device=dev)
         sx, sw = 0.02, 0.003
+        flops = 2.0 * M * N * K
 
         def run():
             coat.coat_fp8_linear_group_quantize(xq, sx, wq, sw, G, q, S, stream=stream)
 
-        for _ in range(3):
-            run()
-        torch.cuda.synchronize()
-        coat.coat_kernel_wait_timeouts(reset=True)
-        # enough launches for half a second of clock samples
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        ev[0].record(stream)
-        for _ in range(5):
-            run()
-        ev[1].record(stream)
-        torch.cuda.synchronize()
-        reps = max(20, int(500.0 / max(ev[0].elapsed_time(ev[1]) / 5, 1e-3)))
-        clocks = ClockSampler(0)
-        clocks.start()
-        ev[0].record(stream)
-        for _ in range(reps):
-            run()
-        ev[1].record(stream)
-        torch.cuda.synchronize()
-        clk = clocks.stop()
-        ms = ev[0].elapsed_time(ev[1]) / reps
-        timeouts = coat.coat_kernel_wait_timeouts(reset=True)
-        flops = 2.0 * M * N * K
-        tf = flops / (ms / 1e3) / 1e12
-        lib_ms = None
+        lib = None
         try:
             a8, b8 = xq.view(torch.float8_e4m3fn), wq.view(torch.float8_e4m3fn)
             one = torch.ones((), device=dev)
-            for _ in range(3):
+
+            def run_lib():
                 torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
-            torch.cuda.synchronize()
-            ev[0].record(stream)
-            for _ in range(20):
-                torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
-            ev[1].record(stream)
-            torch.cuda.synchronize()
-            lib_ms = ev[0].elapsed_time(ev[1]) / 20
+
+            timed(run_lib, 3)
+            lib_ms = timed(run_lib, 20)
+            lib = {"what": "torch._scaled_mm, bf16 output, no group quantization, burst",
+                   "ms": lib_ms, "tflops": flops / (lib_ms / 1e3) / 1e12}
         except (RuntimeError, AttributeError, TypeError):
             pass
+        timed(run, 3)
+        coat.coat_kernel_wait_timeouts(reset=True)
+        ms_b = timed(run, 20)
+        tf_b = flops / (ms_b / 1e3) / 1e12
+        reps = max(20, int(500.0 / max(ms_b, 1e-3)))   # half a second of clock samples
+        clocks = ClockSampler(0)
+        clocks.start()
+        ms_s = timed(run, reps)
+        clk = clocks.stop()
+        tf_s = flops / (ms_s / 1e3) / 1e12
+        timeouts = coat.coat_kernel_wait_timeouts(reset=True)
         print(json.dumps({
             "report": "linear", "layer": name, "M": M, "N": N, "K": K, "G": G,
-            "metric": "fp8_linear_group_quantize_tflops", "value": tf, "unit": "TFLOP/s",
-            "ms": ms, "launches_timed": reps, "data": "synthetic E4M3 codes (activation-like magnitudes)",
+            "metric": "fp8_linear_group_quantize_tflops", "value": tf_b, "unit": "TFLOP/s",
+            "ms": ms_b, "data": "synthetic E4M3 codes (activation-like magnitudes)",
             "dtype": "e4m3 x e4m3 -> f32 accumulate -> e4m3 codes + f32 group scales",
-            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tf / peak, "peak_kind": peak_kind,
+            "roofline": {"bound": "tensor", "achieved": tf_b, "peak": peak_b, "unit": "TFLOP/s",
+                         "frac": tf_b / peak_b, "peak_kind": peak_kind + ", burst",
                          "traffic": None, "kernel": "linear_fp8_kernel"},
+            "sustained": {"launches": reps, "ms": ms_s, "tflops": tf_s, "peak": peak_s,
+                          "frac": tf_s / peak_s, "clocks": clk},
             "output_bytes": M * N + 4 * (M * N // G),
-            "library_fp8_gemm": None if lib_ms is None else {
-                "what": "torch._scaled_mm, bf16 output, no group quantization",
-                "ms": lib_ms, "tflops": flops / (lib_ms / 1e3) / 1e12},
-            "wait_timeouts": timeouts, "clocks": clk}), flush=True)
+            "library_fp8_gemm": lib, "wait_timeouts": timeouts}), flush=True)
 
 
 def report_g_sweep(args):

@@ -208,6 +208,33 @@ __device__ __forceinline__ float dequant_code(const float2* s_L, uint32_t code, 
     return __uint_as_float(__float_as_uint(x) | ((code & 0x80u) << 24));
 }
 
+// The four codes of a packed word, all of one group whose P is a normal
+// float: dequant_code's arithmetic two codes per packed f32x2 instruction
+// (each half rounds like the scalar instruction, so the values are the same),
+// -p formed directly as L (-1/k)_hi, zero magnitudes selected at the end.
+__device__ __forceinline__ float4 dequant_word(const float2* s_L, uint32_t w, const DequantGroup& d) {
+    const float2 L[4] = {s_L[w & 0x7Fu], s_L[(w >> 8) & 0x7Fu], s_L[(w >> 16) & 0x7Fu], s_L[(w >> 24) & 0x7Fu]};
+    const uint64_t rh = pk(d.rk_hi, d.rk_hi), rl = pk(d.rk_lo, d.rk_lo), nrh = pk(-d.rk_hi, -d.rk_hi);
+    const uint64_t ln2 = pk(0.693147182f, 0.693147182f), P = pk(d.P, d.P);
+    float x[4];
+#pragma unroll
+    for (int h = 0; h < 4; h += 2) {
+        const uint64_t lx = pk(L[h].x, L[h + 1].x), ly = pk(L[h].y, L[h + 1].y);
+        const uint64_t np = mul2(lx, nrh);                                 // -p, exactly
+        const uint64_t t = fma2(lx, rl, fma2(ly, rh, fma2(lx, rh, np)));
+        float n0, n1;
+        upk(np, n0, n1);
+        const uint64_t y = pk(ex2_ftz(-n0), ex2_ftz(-n1));
+        upk(mul2(P, fma2(y, mul2(t, ln2), y)), x[h], x[h + 1]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t code = (w >> (8 * j)) & 0xFFu;
+        x[j] = (code & 0x7Fu) ? __uint_as_float(__float_as_uint(x[j]) | ((code & 0x80u) << 24)) : 0.0f;
+    }
+    return make_float4(x[0], x[1], x[2], x[3]);
+}
+
 // Two 16-code chunks per thread (a CTA covers 2 x 4096 codes): the loads of
 // both are issued before any arithmetic, so twice the bytes are in flight
 // per thread (the per-code arithmetic is a dependent chain of ~15 operations).
@@ -275,8 +302,17 @@ dre_dequantize_kernel(const DequantArgs a) {
         }
         float x[kVec];
 #pragma unroll
-        for (int e = 0; e < kVec; ++e)
-            x[e] = dequant_code(s_L, (q[c][e / 4] >> (8 * (e & 3))) & 0xFFu, d[e / Gm::kElems]);
+        for (int i = 0; i < kVec / 4; ++i) {
+            const DequantGroup& dw = d[(4 * i) / Gm::kElems];
+            if (Gm::kElems >= 4 && dw.P > 0.0f) {   // the word's four codes share one group
+                const float4 v = dequant_word(s_L, q[c][i], dw);
+                x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    x[4 * i + j] = dequant_code(s_L, (q[c][i] >> (8 * j)) & 0xFFu, d[(4 * i + j) / Gm::kElems]);
+            }
+        }
         if (full[c]) {
             float4* xp = reinterpret_cast<float4*>(a.x + base[c]);
 #pragma unroll
@@ -343,8 +379,13 @@ dre_dequantize_rows_kernel(const DequantArgs a) {
         if (b >= a.n) break;
         const DequantGroup& d = s_d[(row * 128 + 4 * lane) / G];
         float x[4];
+        if (d.P > 0.0f) {
+            const float4 v = dequant_word(s_L, q[r], d);
+            x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+        } else {   // an all-zero group, or P outside the normal range
 #pragma unroll
-        for (int j = 0; j < 4; ++j) x[j] = dequant_code(s_L, (q[r] >> (8 * j)) & 0xFFu, d);
+            for (int j = 0; j < 4; ++j) x[j] = dequant_code(s_L, (q[r] >> (8 * j)) & 0xFFu, d);
+        }
         if (b + 4 <= a.n) {
             st_cs(reinterpret_cast<float4*>(a.x + b), make_float4(x[0], x[1], x[2], x[3]));
         } else {

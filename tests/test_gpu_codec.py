@@ -86,7 +86,7 @@ def _dequant_ok(xg, xo):
         (np.abs(xo) < 2.0 ** -126) & (err <= SUBNORMAL_STEP))
 
 
-@pytest.mark.parametrize("G", [1, 16, 128, 256])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16, 128, 256])
 def test_dequantize_matches_oracle(G):
     x = _groups(G, max(64, 8192 // G), seed=100 + G)
     q, S, k = oracle.dre_quantize(x, G)
