@@ -27,6 +27,7 @@
 // next tile accumulates.  Every wait on an mbarrier is bounded: when one gives up,
 // the kernel counts it in g_wait_timeouts, lets its copies and MMAs in flight
 // finish, frees its tensor memory and returns.
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>   // CUtensorMap and its enums; the encoder is fetched at run time
 
@@ -523,13 +524,26 @@ bool encode_operand(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Per device and G: the number of CTA pairs that fit at once, a property of
+// the device and the kernel (0 = not known yet; set once, read without a lock:
+// a race only repeats the same host-side query).  The shared-memory attribute
+// is set on every launch, since a device reset clears it.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_pairs[kMaxDevices][5];
+
+int g_index(int G) { return G == 8 ? 0 : G == 16 ? 1 : G == 32 ? 2 : G == 64 ? 3 : 4; }
+
 template <int G>
 cudaError_t launch_linear_g(const LinArgs& a, cudaStream_t s) {
     alignas(64) CUtensorMap tmx, tmw;
     if (!encode_operand(&tmx, a.xq, a.M, a.K, kBM) || !encode_operand(&tmw, a.wq, a.N, a.K, kBNh))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(linear_fp8_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::atomic<int>* cached = (dev >= 0 && dev < kMaxDevices) ? &g_pairs[dev][g_index(G)] : nullptr;
+    int clusters = cached ? cached->load(std::memory_order_relaxed) : 0;
+    e = cudaFuncSetAttribute(linear_fp8_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -543,9 +557,11 @@ cudaError_t launch_linear_g(const LinArgs& a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(2);
-    int clusters = 0;   // CTA pairs that fit on the GPU at once
-    if ((e = cudaOccupancyMaxActiveClusters(&clusters, linear_fp8_kernel<G>, &cfg)) != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    if (clusters < 1) {   // first launch on this device
+        if ((e = cudaOccupancyMaxActiveClusters(&clusters, linear_fp8_kernel<G>, &cfg)) != cudaSuccess) return e;
+        if (clusters < 1) return cudaErrorInvalidConfiguration;
+        if (cached) cached->store(clusters, std::memory_order_relaxed);
+    }
     const int64_t tiles = ((a.M + 2 * kBM - 1) / (2 * kBM)) * ((a.N + kBN - 1) / kBN);
     cfg.gridDim = dim3(2u * (unsigned)(tiles < clusters ? tiles : clusters));
     e = cudaLaunchKernelEx(&cfg, linear_fp8_kernel<G>, tmx, tmw, a);
