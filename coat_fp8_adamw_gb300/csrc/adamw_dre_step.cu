@@ -135,6 +135,32 @@ __device__ __forceinline__ void load_chunk(const StepArgs& a, int64_t base, bool
     }
 }
 
+// The gradients and one moment's codes of the 16 parameters from `b`, read
+// again from global memory (zero beyond n), as load_chunk packed them.
+__device__ __forceinline__ void reload_inputs(const StepArgs& a, int64_t b, bool second, uint32_t* gw,
+                                              uint32_t* cw) {
+    const uint8_t* q = second ? a.vq : a.mq;
+    if (b + kVec <= a.n) {
+        const uint4* gp = reinterpret_cast<const uint4*>(a.g + b);
+        const uint4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
+        const uint4 cc = __ldcg(reinterpret_cast<const uint4*>(q + b));
+        gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
+        gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
+        cw[0] = cc.x; cw[1] = cc.y; cw[2] = cc.z; cw[3] = cc.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < kVec / 2; ++i) gw[i] = 0u;
+#pragma unroll
+        for (int i = 0; i < kVec / 4; ++i) cw[i] = 0u;
+        for (int e = 0; e < kVec; ++e) {
+            if (b + e < a.n) {
+                gw[e / 2] |= (uint32_t)a.g[b + e] << (16 * (e & 1));
+                cw[e / 4] |= (uint32_t)q[b + e] << (8 * (e & 3));
+            }
+        }
+    }
+}
+
 // Bulk prefetch of `bytes` (a multiple of 16) at a 16-byte aligned address into
 // L2 (cp.async.bulk.prefetch: no registers, no shared memory, no completion
 // to wait for).
@@ -450,8 +476,12 @@ struct CtaLayout {
     static constexpr int L = G / kVec;          // lanes per group
     static constexpr size_t off_m = 0;
     static constexpr size_t off_v = off_m + (size_t)CTA * kVec * 4;
+    // The exact pass's inputs (each thread's gradients and codes) are stashed in
+    // shared memory for G >= 128; for smaller groups the exact pass reads them
+    // again from global memory (L2), so that more CTAs fit per SM.
+    static constexpr bool kStash = G >= 128;
     static constexpr size_t off_in = off_v + (size_t)CTA * kVec * 4;   // g, m codes, v codes per thread
-    static constexpr size_t off_grp = off_in + (size_t)CTA * 64;
+    static constexpr size_t off_grp = off_in + (kStash ? (size_t)CTA * 64 : 0);
     static constexpr size_t off_lg = off_grp + (size_t)NGC * sizeof(GroupRec);
     static constexpr size_t bytes = off_lg + 128 * 4;
 };
@@ -561,10 +591,12 @@ step_kernel_cta(const StepArgs a) {
         }
         if (active) store_w(a, base, full, c);
         // the inputs of the exact pass: this thread's gradients and codes
-        sm_in[4 * tid + 0] = make_uint4(c.g[0], c.g[1], c.g[2], c.g[3]);
-        sm_in[4 * tid + 1] = make_uint4(c.g[4], c.g[5], c.g[6], c.g[7]);
-        sm_in[4 * tid + 2] = make_uint4(c.mq[0], c.mq[1], c.mq[2], c.mq[3]);
-        sm_in[4 * tid + 3] = make_uint4(c.vq[0], c.vq[1], c.vq[2], c.vq[3]);
+        if constexpr (Lay::kStash) {
+            sm_in[4 * tid + 0] = make_uint4(c.g[0], c.g[1], c.g[2], c.g[3]);
+            sm_in[4 * tid + 1] = make_uint4(c.g[4], c.g[5], c.g[6], c.g[7]);
+            sm_in[4 * tid + 2] = make_uint4(c.mq[0], c.mq[1], c.mq[2], c.mq[3]);
+            sm_in[4 * tid + 3] = make_uint4(c.vq[0], c.vq[1], c.vq[2], c.vq[3]);
+        }
 
         // smallest non-zero values as keys; a lane holding an exact zero (rare:
         // both inputs of an element zero, or a fast sum that cancels) rescans
@@ -661,14 +693,16 @@ step_kernel_cta(const StepArgs a) {
             h &= h - 1u;
             const int th = (int)r.hwarp * 32 + ln;
             float* vals = second ? sm_v[th] : sm_m[th];
-            // the holder's gradients and codes, from shared memory (zero beyond n)
+            // the holder's gradients and codes (zero beyond n)
             uint32_t gw[8], cw[4];
-            {
+            if constexpr (Lay::kStash) {
                 const uint4 g0 = sm_in[4 * th], g1 = sm_in[4 * th + 1];
                 const uint4 cc = sm_in[4 * th + (second ? 3 : 2)];
                 gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
                 gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
                 cw[0] = cc.x; cw[1] = cc.y; cw[2] = cc.z; cw[3] = cc.w;
+            } else {
+                reload_inputs(a, cta_base + (int64_t)th * kVec, second, gw, cw);
             }
             uint32_t msk = 0u;
             if constexpr (kStatBlocks) {
