@@ -235,9 +235,11 @@ __device__ __forceinline__ StateParams state_params(float S, float k, const df::
 // For k = 1 the power is the plain product |E4M3(q)| S, which is often a
 // rounding tie: it is formed by one correctly rounded multiplication.
 // Otherwise the power is rounded with certainty (float64 in the rare case
-// where the double-float value lies too near an fp32 rounding midpoint).
+// where the double-float value lies too near an fp32 rounding midpoint; only
+// that case calls k_of() for the stored exponent).
+template <typename KOf>
 __device__ __forceinline__ float exact_moment(uint32_t code, float gf, bool second, F2 A, F2 rkd,
-                                              float S, float k, float beta, float omb,
+                                              float S, KOf k_of, float beta, float omb,
                                               const df::Tables& t, const float* lg_hi,
                                               const float* lg_lo) {
     float prev = 0.0f;
@@ -248,8 +250,11 @@ __device__ __forceinline__ float exact_moment(uint32_t code, float gf, bool seco
         } else {
             const F2 L = {lg_hi[mag], lg_lo[mag]};
             bool slow = false;
-            prev = df::dequant_certain(L, A, rkd, e4m3_value(mag), S, k, t, slow);
-            if (slow) atomicAdd(&g_recompute[0], 1ull);
+            prev = df::dequant_try(L, A, rkd, t, slow);
+            if (slow) {
+                prev = df::dequant_f64(e4m3_value(mag), S, k_of());
+                atomicAdd(&g_recompute[0], 1ull);
+            }
         }
         if (code & 0x80u) prev = -prev;
     }
@@ -448,20 +453,57 @@ __device__ __forceinline__ bool cand(float x, float gabs, uint32_t code, const C
 struct GroupRec {
     F2 A[2];             // log2(448 S) of the stored m (0) and v (1)
     F2 rkd[2];           // 1/k
+    F2 lex[4];           // log2 of the exact extremes
     float P[2];          // fast-path factor
     float S[2];          // stored S
-    float kst[2];        // stored k
-    float eps[2];        // fast-path error bound
     float fmx[2];        // fast max |m|, max v
     float fmn[2];        // fast smallest non-zero
     float gmx;           // max |g|
     uint32_t hwarp;      // warp holding the group
     uint32_t holders[4]; // lanes holding candidates, per statistic
     float ex[4];         // exact extremes
-    F2 lex[4];           // their log2
     float k[2];          // fresh k
     float inv[2];        // encoding constants
     float cz[2];
+};
+
+// The records of a CTA's N groups in shared memory, either as an array of
+// GroupRec or (kSoA) as a structure of arrays.  The per-group jobs of G <= 32
+// run one group per lane (statistic blocks): lanes then read one field of
+// consecutive groups, which the structure of arrays puts in consecutive words;
+// for larger G the four jobs of a group sit on adjacent lanes and read
+// neighbouring fields of one record.
+template <int N, bool kSoA>
+struct GroupRecs {
+    unsigned char* p;
+#define COAT_REC_FIELD(T, name, M)                                                                   \
+    __device__ __forceinline__ T& name(int m, int i) const {                                        \
+        if constexpr (kSoA)                                                                          \
+            return reinterpret_cast<T*>(p + (size_t)N * offsetof(GroupRec, name))[m * N + i];         \
+        else                                                                                         \
+            return reinterpret_cast<GroupRec*>(p)[i].name[m];                                        \
+    }
+    COAT_REC_FIELD(F2, A, 2)
+    COAT_REC_FIELD(F2, rkd, 2)
+    COAT_REC_FIELD(F2, lex, 4)
+    COAT_REC_FIELD(float, P, 2)
+    COAT_REC_FIELD(float, S, 2)
+    COAT_REC_FIELD(float, fmx, 2)
+    COAT_REC_FIELD(float, fmn, 2)
+    COAT_REC_FIELD(uint32_t, holders, 4)
+    COAT_REC_FIELD(float, ex, 4)
+    COAT_REC_FIELD(float, k, 2)
+    COAT_REC_FIELD(float, inv, 2)
+    COAT_REC_FIELD(float, cz, 2)
+#undef COAT_REC_FIELD
+    __device__ __forceinline__ float& gmx(int i) const {
+        if constexpr (kSoA) return reinterpret_cast<float*>(p + (size_t)N * offsetof(GroupRec, gmx))[i];
+        else return reinterpret_cast<GroupRec*>(p)[i].gmx;
+    }
+    __device__ __forceinline__ uint32_t& hwarp(int i) const {
+        if constexpr (kSoA) return reinterpret_cast<uint32_t*>(p + (size_t)N * offsetof(GroupRec, hwarp))[i];
+        else return reinterpret_cast<GroupRec*>(p)[i].hwarp;
+    }
 };
 
 // Moment rows: 16 floats per thread, the four 16-byte chunks of thread t
@@ -500,7 +542,7 @@ step_kernel_cta(const StepArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     float(*sm_m)[kVec] = reinterpret_cast<float(*)[kVec]>(smem + Lay::off_m);
     float(*sm_v)[kVec] = reinterpret_cast<float(*)[kVec]>(smem + Lay::off_v);
-    GroupRec* grp = reinterpret_cast<GroupRec*>(smem + Lay::off_grp);
+    const GroupRecs<NGC, (NGC >= 64)> R{smem + Lay::off_grp};   // structure of arrays with statistic blocks
     uint4* sm_in = reinterpret_cast<uint4*>(smem + Lay::off_in);   // 4 x 16 bytes per thread
     float* lg_hi = reinterpret_cast<float*>(smem + Lay::off_lg);
     const float* lg_lo = reinterpret_cast<const float*>(gtab::kLog2Frac448Lo);
@@ -552,13 +594,11 @@ step_kernel_cta(const StepArgs a) {
         const int gi = j >> 1, sm_ = j & 1;
         const float S = bsk[i].x, k = bsk[i].y;
         const StateParams p = state_params(S, k, tab);
-        GroupRec& r = grp[gi];
-        r.A[sm_] = p.A;
-        r.rkd[sm_] = p.rkd;
-        r.P[sm_] = p.P;
-        r.S[sm_] = S;
-        r.kst[sm_] = k;
-        r.eps[sm_] = fast_err(p.rkd.hi);
+        const int ri = gi;
+        R.A(sm_, ri) = p.A;
+        R.rkd(sm_, ri) = p.rkd;
+        R.P(sm_, ri) = p.P;
+        R.S(sm_, ri) = S;
     }
     __syncthreads();
 
@@ -566,9 +606,9 @@ step_kernel_cta(const StepArgs a) {
     const int gi = (tid * kVec) / G;
     const int lig = (tid * kVec % G) / kVec;   // lane within the group
     {
-        const GroupRec& r = grp[gi];
-        const float Pm = r.P[0], rkm = r.rkd[0].hi, rkv = r.rkd[1].hi;
-        const float bPm = a.beta1 * Pm, bPv = a.beta2 * r.P[1];
+        const int ri = gi;
+        const float Pm = R.P(0, ri), rkm = R.rkd(0, ri).hi, rkv = R.rkd(1, ri).hi;
+        const float bPm = a.beta1 * Pm, bPv = a.beta2 * R.P(1, ri);
         float lmx_m = 0.0f, lmx_v = 0.0f, lmx_g = 0.0f;
         float lmn_m = kInf, lmn_v = kInf;   // smallest |m| and v, zeros included
 #pragma unroll
@@ -625,10 +665,10 @@ step_kernel_cta(const StepArgs a) {
             fmn_v = fminf(fmn_v, __shfl_xor_sync(kFull, fmn_v, off));
         }
         const float fmn_mv = nz_key_value(fmn_m), fmn_vv = nz_key_value(fmn_v);
-        const GroupWin win = make_win(a, Pm, r.eps[0], r.eps[1], fmx_m, fmn_mv, fmx_v, fmn_vv, gmx);
+        const GroupWin win = make_win(a, Pm, fast_err(rkm), fast_err(rkv), fmx_m, fmn_mv, fmx_v, fmn_vv, gmx);
         // lane-level tests: sufficient conditions for holding a candidate.  A
         // lane with a fast zero holds one when the group has a non-zero input.
-        const bool live_m = win.T > 0.0f, live_v = r.P[1] > 0.0f || gmx > 0.0f;
+        const bool live_m = win.T > 0.0f, live_v = R.P(1, ri) > 0.0f || gmx > 0.0f;
         const float lmn_mv = nz_key_value(lmn_m), lmn_vv = nz_key_value(lmn_v);
         const float Tl = fmaf(2.0f * a.omb1, lmx_g, lmx_m);   // >= T_j of every element here
         const bool c1 = (lmn_mv > 0.0f &&
@@ -642,17 +682,16 @@ step_kernel_cta(const StepArgs a) {
         const uint32_t h3 = __ballot_sync(kFull, (lmn_vv > 0.0f && lmn_vv <= win.lo_v) ||
                                                      (lz == 0.0f && live_v)) & gmask;
         if (lig == 0) {
-            GroupRec& rw = grp[gi];
-            rw.fmx[0] = fmx_m;
-            rw.fmx[1] = fmx_v;
-            rw.fmn[0] = fmn_mv;
-            rw.fmn[1] = fmn_vv;
-            rw.gmx = gmx;
-            rw.hwarp = (uint32_t)warp;
-            rw.holders[0] = h0;
-            rw.holders[1] = h1;
-            rw.holders[2] = h2;
-            rw.holders[3] = h3;
+            R.fmx(0, ri) = fmx_m;
+            R.fmx(1, ri) = fmx_v;
+            R.fmn(0, ri) = fmn_mv;
+            R.fmn(1, ri) = fmn_vv;
+            R.gmx(ri) = gmx;
+            R.hwarp(ri) = (uint32_t)warp;
+            R.holders(0, ri) = h0;
+            R.holders(1, ri) = h1;
+            R.holders(2, ri) = h2;
+            R.holders(3, ri) = h3;
         }
     }
     __syncthreads();
@@ -677,21 +716,25 @@ step_kernel_cta(const StepArgs a) {
             jg = j >> 2;
             s = j & 3;
         }
-        GroupRec& r = grp[jg];
+        const int ri = jg;
         const bool second = s >= 2, is_max = (s & 1) == 0;
         const int sm_ = second ? 1 : 0;
-        const GroupWin win = make_win(a, r.P[0], r.eps[0], r.eps[1], r.fmx[0], r.fmn[0], r.fmx[1],
-                                      r.fmn[1], r.gmx);
+        const GroupWin win = make_win(a, R.P(0, ri), fast_err(R.rkd(0, ri).hi), fast_err(R.rkd(1, ri).hi), R.fmx(0, ri), R.fmn(0, ri), R.fmx(1, ri),
+                                      R.fmn(1, ri), R.gmx(ri));
         const CandTest ct = cand_test(win, s, a.omb1);
-        const F2 A = r.A[sm_], rkd = r.rkd[sm_];
-        const float S = r.S[sm_], kst = r.kst[sm_];
+        const F2 A = R.A(sm_, ri), rkd = R.rkd(sm_, ri);
+        const float S = R.S(sm_, ri);
+        // the stored k, read again from the record in global memory (E of this
+        // CTA overwrites it only after this phase) in the rare float64 case
+        const float* kst_at = reinterpret_cast<const float*>(a.meta + g_first + jg) + 2 * sm_ + 1;
+        const auto kst = [kst_at]() { return *kst_at; };
         const float beta = second ? a.beta2 : a.beta1, omb = second ? a.omb2 : a.omb1;
         float best = is_max ? 0.0f : kInf;
-        uint32_t h = r.holders[s];
+        uint32_t h = R.holders(s, ri);
         while (h) {
             const int ln = __ffs(h) - 1;
             h &= h - 1u;
-            const int th = (int)r.hwarp * 32 + ln;
+            const int th = (int)R.hwarp(ri) * 32 + ln;
             float* vals = second ? sm_v[th] : sm_m[th];
             // the holder's gradients and codes (zero beyond n)
             uint32_t gw[8], cw[4];
@@ -780,23 +823,23 @@ step_kernel_cta(const StepArgs a) {
             }
         }
         best = (best < kInf) ? best : 0.0f;
-        r.ex[s] = best;
-        r.lex[s] = best > 0.0f ? df::log2_df(best, tab) : F2{0.0f, 0.0f};
+        R.ex(s, ri) = best;
+        R.lex(s, ri) = best > 0.0f ? df::log2_df(best, tab) : F2{0.0f, 0.0f};
     }
     __syncthreads();
 
     // ---- E: fresh k, S, encoding constants and the group record ----
     for (int j = tid; j < 2 * NGC; j += kCta) {
         const int jg = j >> 1, sm_ = j & 1;
-        GroupRec& r = grp[jg];
-        const float mx = r.ex[2 * sm_], mn = r.ex[2 * sm_ + 1];
+        const int ri = jg;
+        const float mx = R.ex(2 * sm_, ri), mn = R.ex(2 * sm_ + 1, ri);
         float k, S;
-        k_and_S_logs(mx, mn, r.lex[2 * sm_], r.lex[2 * sm_ + 1], tab, k, S);
+        k_and_S_logs(mx, mn, R.lex(2 * sm_, ri), R.lex(2 * sm_ + 1, ri), tab, k, S);
         float inv, cz;
         encode_consts(mx, k, inv, cz);
-        r.k[sm_] = k;
-        r.inv[sm_] = inv;
-        r.cz[sm_] = cz;
+        R.k(sm_, ri) = k;
+        R.inv(sm_, ri) = inv;
+        R.cz(sm_, ri) = cz;
         const int64_t gg = g_first + jg;
         if (gg * G < a.n) reinterpret_cast<float2*>(a.meta + gg)[sm_] = make_float2(S, k);
     }
@@ -805,9 +848,9 @@ step_kernel_cta(const StepArgs a) {
     // ---- F: encode and store the codes ----
     if (!active) return;
     {
-        const GroupRec& r = grp[gi];
-        const float km = r.k[0], invm = r.inv[0], czm = r.cz[0];
-        const float kv = r.k[1], invv = r.inv[1], czv = r.cz[1];
+        const int ri = gi;
+        const float km = R.k(0, ri), invm = R.inv(0, ri), czm = R.cz(0, ri);
+        const float kv = R.k(1, ri), invv = R.inv(1, ri), czv = R.cz(1, ri);
         uint32_t om[4], ov[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -895,14 +938,16 @@ step_kernel_thread(const StepArgs a) {
             const bool cv = cand(v[e], fabsf(gf), cvq, cand_test(win, 2, a.omb1)) ||
                             cand(v[e], fabsf(gf), cvq, cand_test(win, 3, a.omb1));
             if (cm) {
-                m[e] = exact_moment(byte_of(c.mq, e), gf, false, pm.A, pm.rkd, pm.S, md.y,
+                m[e] = exact_moment(byte_of(c.mq, e), gf, false, pm.A, pm.rkd, pm.S,
+                                    [k = md.y]() { return k; },
                                     a.beta1, a.omb1, tab, lg_hi, lg_lo);
                 const float ax = fabsf(m[e]);
                 ex[0] = fmaxf(ex[0], ax);
                 if (ax > 0.0f) ex[1] = fminf(ex[1], ax);
             }
             if (cv) {
-                v[e] = exact_moment(byte_of(c.vq, e), gf, true, pv.A, pv.rkd, pv.S, md.w,
+                v[e] = exact_moment(byte_of(c.vq, e), gf, true, pv.A, pv.rkd, pv.S,
+                                    [k = md.w]() { return k; },
                                     a.beta2, a.omb2, tab, lg_hi, lg_lo);
                 const float ax = fabsf(v[e]);
                 ex[2] = fmaxf(ex[2], ax);

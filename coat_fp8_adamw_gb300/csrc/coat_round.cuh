@@ -101,9 +101,9 @@ COAT_HD float k_err_bound(float lmx_abs, float lmn_abs, float d_abs) {
 // certain, else (rarely) the float64 definition.  A result in the fp32
 // subnormal range (scaling it would round twice) also takes the float64 path.
 // `mag` is |E4M3(q)| (> 0), S > 0, k the stored exponent; `slow` reports the
-// float64 path.
-COAT_HD float dequant_certain(F2 L, F2 A, F2 rkd, float mag, float S, float k, const Tables& t,
-                              bool& slow) {
+// float64 path.  dequant_try is the first part alone: the double-float value
+// rounded once, with `slow` set where the caller must take the float64 path.
+COAT_HD float dequant_try(F2 L, F2 A, F2 rkd, const Tables& t, bool& slow) {
     const F2 z = mul22(add2(L, A), rkd);
     int n = 0;
     const F2 m = exp2_df_parts(z, t, n);
@@ -111,6 +111,11 @@ COAT_HD float dequant_certain(F2 L, F2 A, F2 rkd, float mag, float S, float k, c
     const float r = round_certain(m, dequant_err_bound(abs1(z.hi), abs1(A.hi), rkd.hi), certain);
     const float x = scale2(r, n);
     slow = !certain || !(x >= 1.17549435e-38f);
+    return x;
+}
+COAT_HD float dequant_certain(F2 L, F2 A, F2 rkd, float mag, float S, float k, const Tables& t,
+                              bool& slow) {
+    const float x = dequant_try(L, A, rkd, t, slow);
     return slow ? dequant_f64(mag, S, k) : x;
 }
 
