@@ -32,16 +32,14 @@ dre_quantize_kernel(const QuantArgs a) {
     __shared__ SmemTables st;
     __shared__ float s_mx[Gm::kGpc], s_k[Gm::kGpc], s_inv[Gm::kGpc], s_pre[Gm::kGpc];
     __shared__ uint32_t s_mn[Gm::kGpc];
-    load_smem_tables(st, threadIdx.x, kThreads);
-    __syncthreads();
-    const df::Tables tab = tables_of(st);
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t base = tid * kVec;
-    // the job phase below has CTA barriers: only the per-lane form may leave early
-    if (!Gm::kJobs && __all_sync(0xFFFFFFFFu, base >= a.n)) return;
+    // the table fill's barrier below and the job phase's barriers: only the
+    // per-lane form, which has no job phase, may leave before them
     const bool active = base < a.n;
     const bool full = base + kVec <= a.n;
 
+    // the inputs first: their loads are in flight while the tables are filled
     float x[kVec];
     if (active && full) {
         const float4* xp = reinterpret_cast<const float4*>(a.x + base);
@@ -54,6 +52,10 @@ dre_quantize_kernel(const QuantArgs a) {
 #pragma unroll
         for (int e = 0; e < kVec; ++e) x[e] = (active && base + e < a.n) ? a.x[base + e] : 0.0f;
     }
+    load_smem_tables(st, threadIdx.x, kThreads);
+    __syncthreads();
+    const df::Tables tab = tables_of(st);
+    if (!Gm::kJobs && __all_sync(0xFFFFFFFFu, base >= a.n)) return;
 
     float mx[Gm::kGroups];
     uint32_t mn[Gm::kGroups];
