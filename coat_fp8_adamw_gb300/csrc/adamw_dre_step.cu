@@ -706,7 +706,14 @@ step_kernel_cta(const StepArgs a) {
     // block would leave the minimum jobs to a single warp, and the jobs of a
     // group stay on adjacent lanes instead.
     constexpr bool kStatBlocks = NGC >= 64;
-    for (int j = tid; j < 4 * NGC; j += kCta) {
+    // With G >= 128 the 4 NGC jobs fill a half or a quarter of the CTA: each job
+    // takes kSplit adjacent threads that scan every kSplit-th holder lane and
+    // combine their extremes by shuffles, so that a job's holders run side by side.
+    constexpr int kSplitCap = kCta / (4 * NGC);
+    constexpr int kSplit = kSplitCap >= 4 && L >= 4 ? 4 : (kSplitCap >= 2 && L >= 2 ? 2 : 1);
+    static_assert((kSplit * 4 * NGC) % 32 == 0 || kSplit == 1, "whole warps for the shuffles");
+    for (int jt = tid; jt < kSplit * 4 * NGC; jt += kCta) {
+        const int j = jt / kSplit, sub = jt % kSplit;
         int jg, s;
         if constexpr (kStatBlocks) {
             const int blk = j / NGC;
@@ -731,6 +738,13 @@ step_kernel_cta(const StepArgs a) {
         const float beta = second ? a.beta2 : a.beta1, omb = second ? a.omb2 : a.omb1;
         float best = is_max ? 0.0f : kInf;
         uint32_t h = R.holders(s, ri);
+        if constexpr (kSplit > 1) {   // every kSplit-th holder lane for each thread of the job
+            uint32_t mine = 0u;
+            int k = 0;
+            for (uint32_t t = h; t; t &= t - 1u, ++k)
+                if ((k & (kSplit - 1)) == sub) mine |= t & (0u - t);
+            h = mine;
+        }
         while (h) {
             const int ln = __ffs(h) - 1;
             h &= h - 1u;
@@ -821,6 +835,14 @@ step_kernel_cta(const StepArgs a) {
                 if (is_max) best = fmaxf(best, ax);
                 else if (ax > 0.0f) best = fminf(best, ax);
             }
+        }
+        if constexpr (kSplit > 1) {
+#pragma unroll
+            for (int off = 1; off < kSplit; off <<= 1) {
+                const float ob = __shfl_xor_sync(kFull, best, off);
+                best = is_max ? fmaxf(best, ob) : fminf(best, ob);
+            }
+            if (sub != 0) continue;
         }
         best = (best < kInf) ? best : 0.0f;
         R.ex(s, ri) = best;
