@@ -30,12 +30,13 @@
 // re-evaluated elements are encoded from their exact values.
 //
 // Execution.  A CTA of 128 threads owns 2048 consecutive parameters (16 per
-// thread: every stream is whole 128-bit accesses); eight CTAs share an SM.
-// The per-group work runs as CTA-wide jobs between barriers -- one thread per
-// (group, moment) or per (group, statistic) -- so that it occupies a few full
-// warps instead of a few lanes of every warp.  The moments wait in shared
-// memory between phases, next to a copy of each thread's gradients and codes
-// for the exact pass.
+// thread: every stream is whole 128-bit accesses); up to eight CTAs share an
+// SM.  The per-group work runs as CTA-wide jobs between barriers -- one thread
+// per (group, moment), and one to four threads per (group, statistic) -- so
+// that it occupies a few full warps instead of a few lanes of every warp.  The
+// moments wait in shared memory between phases (for G >= 128 next to a copy of
+// each thread's gradients and codes for the exact pass; smaller groups read
+// those again from L2 so that more CTAs fit).
 //   B  stored-state parameters                      2 jobs per group
 //   C  fast path, statistics, candidate holders      every thread
 //   D  candidate masks and exact re-evaluation       4 jobs per group
