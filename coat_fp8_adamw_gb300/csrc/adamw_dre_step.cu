@@ -707,16 +707,24 @@ step_kernel_cta(const StepArgs a) {
     // block would leave the minimum jobs to a single warp, and the jobs of a
     // group stay on adjacent lanes instead.
     constexpr bool kStatBlocks = NGC >= 64;
-    // With G >= 128 the 4 NGC jobs fill a half or a quarter of the CTA: each job
-    // takes kSplit adjacent threads that scan every kSplit-th holder lane and
-    // combine their extremes by shuffles, so that a job's holders run side by side.
-    constexpr int kSplitCap = kCta / (4 * NGC);
-    constexpr int kSplit = kSplitCap >= 4 && L >= 4 ? 4 : (kSplitCap >= 2 && L >= 2 ? 2 : 1);
-    static_assert((kSplit * 4 * NGC) % 32 == 0 || kSplit == 1, "whole warps for the shuffles");
-    for (int jt = tid; jt < kSplit * 4 * NGC; jt += kCta) {
-        const int j = jt / kSplit, sub = jt % kSplit;
-        int jg, s;
-        if constexpr (kStatBlocks) {
+    // With G >= 128 the 4 NGC jobs would leave half or more of the CTA idle:
+    // a group gets kT = 128 / NGC threads instead (8 or 16).  Its lanes 0, 1, 2
+    // take max|m|, max v and min v, whose windows admit one holder lane almost
+    // always; the other kT - 3 share the holder lanes of min|m| (partial
+    // cancellation puts two or three lanes in its window), scanning every
+    // (kT - 3)-th of them, and combine their minima by shuffles over the kT lanes.
+    constexpr int kT = (kCta % NGC == 0) ? kCta / NGC : 0;
+    constexpr bool kAsym = kT >= 8 && L >= 4;
+    static_assert(!kAsym || (32 % kT == 0 && kT * NGC == kCta), "a group's lanes within one warp");
+    for (int jt = tid; jt < (kAsym ? kCta : 4 * NGC); jt += kCta) {
+        const int j = jt;
+        int jg, s, sub = 0, nsub = 1;
+        if constexpr (kAsym) {
+            jg = jt / kT;
+            const int r = jt % kT;
+            s = r == 0 ? 0 : (r == 1 ? 2 : (r == 2 ? 3 : 1));
+            if (r >= 3) { sub = r - 3; nsub = kT - 3; }
+        } else if constexpr (kStatBlocks) {
             const int blk = j / NGC;
             jg = j - blk * NGC;
             s = blk == 0 ? 0 : (blk == 1 ? 2 : (blk == 2 ? 1 : 3));
@@ -739,11 +747,11 @@ step_kernel_cta(const StepArgs a) {
         const float beta = second ? a.beta2 : a.beta1, omb = second ? a.omb2 : a.omb1;
         float best = is_max ? 0.0f : kInf;
         uint32_t h = R.holders(s, ri);
-        if constexpr (kSplit > 1) {   // every kSplit-th holder lane for each thread of the job
+        if (nsub > 1) {   // every nsub-th holder lane for this thread of the job
             uint32_t mine = 0u;
             int k = 0;
             for (uint32_t t = h; t; t &= t - 1u, ++k)
-                if ((k & (kSplit - 1)) == sub) mine |= t & (0u - t);
+                if (k % nsub == sub) mine |= t & (0u - t);
             h = mine;
         }
         while (h) {
@@ -837,13 +845,13 @@ step_kernel_cta(const StepArgs a) {
                 else if (ax > 0.0f) best = fminf(best, ax);
             }
         }
-        if constexpr (kSplit > 1) {
+        if constexpr (kAsym) {
+            const int r = jt % kT;
+            float mm = r >= 3 ? best : kInf;
 #pragma unroll
-            for (int off = 1; off < kSplit; off <<= 1) {
-                const float ob = __shfl_xor_sync(kFull, best, off);
-                best = is_max ? fmaxf(best, ob) : fminf(best, ob);
-            }
-            if (sub != 0) continue;
+            for (int off = 1; off < kT; off <<= 1) mm = fminf(mm, __shfl_xor_sync(kFull, mm, off));
+            if (r > 3) continue;
+            if (r == 3) best = mm;
         }
         best = (best < kInf) ? best : 0.0f;
         R.ex(s, ri) = best;
