@@ -34,9 +34,8 @@
 // SM.  The per-group work runs as CTA-wide jobs between barriers -- one thread
 // per (group, moment), and one to four threads per (group, statistic) -- so
 // that it occupies a few full warps instead of a few lanes of every warp.  The
-// moments wait in shared memory between phases (for G >= 128 next to a copy of
-// each thread's gradients and codes for the exact pass; smaller groups read
-// those again from L2 so that more CTAs fit).
+// moments wait in shared memory between phases; the exact pass reads a holder
+// lane's gradients and codes again from L2.
 //   B  stored-state parameters                      2 jobs per group
 //   C  fast path, statistics, candidate holders      every thread
 //   D  candidate masks and exact re-evaluation       4 jobs per group
@@ -519,12 +518,7 @@ struct CtaLayout {
     static constexpr int L = G / kVec;          // lanes per group
     static constexpr size_t off_m = 0;
     static constexpr size_t off_v = off_m + (size_t)CTA * kVec * 4;
-    // The exact pass's inputs (each thread's gradients and codes) are stashed in
-    // shared memory for G >= 128; for smaller groups the exact pass reads them
-    // again from global memory (L2), so that more CTAs fit per SM.
-    static constexpr bool kStash = G >= 128;
-    static constexpr size_t off_in = off_v + (size_t)CTA * kVec * 4;   // g, m codes, v codes per thread
-    static constexpr size_t off_grp = off_in + (kStash ? (size_t)CTA * 64 : 0);
+    static constexpr size_t off_grp = off_v + (size_t)CTA * kVec * 4;
     static constexpr size_t off_lg = off_grp + (size_t)NGC * sizeof(GroupRec);
     static constexpr size_t bytes = off_lg + 128 * 4;
 };
@@ -538,13 +532,12 @@ step_kernel_cta(const StepArgs a) {
     constexpr int NGC = Lay::NGC;
     constexpr int L = Lay::L;
     static_assert(L >= 1 && L <= 16 && (Lay::off_v % 16) == 0 && (Lay::off_grp % 16) == 0 &&
-                      (Lay::off_in % 16) == 0 && (Lay::off_lg % 4) == 0,
+                      (Lay::off_lg % 4) == 0,
                   "shared-memory layout");
     extern __shared__ __align__(16) unsigned char smem[];
     float(*sm_m)[kVec] = reinterpret_cast<float(*)[kVec]>(smem + Lay::off_m);
     float(*sm_v)[kVec] = reinterpret_cast<float(*)[kVec]>(smem + Lay::off_v);
     const GroupRecs<NGC, (NGC >= 64)> R{smem + Lay::off_grp};   // structure of arrays with statistic blocks
-    uint4* sm_in = reinterpret_cast<uint4*>(smem + Lay::off_in);   // 4 x 16 bytes per thread
     float* lg_hi = reinterpret_cast<float*>(smem + Lay::off_lg);
     const float* lg_lo = reinterpret_cast<const float*>(gtab::kLog2Frac448Lo);
 
@@ -631,13 +624,6 @@ step_kernel_cta(const StepArgs a) {
             *reinterpret_cast<float4*>(&sm_v[tid][slot]) = make_float4(vt[0], vt[1], vt[2], vt[3]);
         }
         if (active) store_w(a, base, full, c);
-        // the inputs of the exact pass: this thread's gradients and codes
-        if constexpr (Lay::kStash) {
-            sm_in[4 * tid + 0] = make_uint4(c.g[0], c.g[1], c.g[2], c.g[3]);
-            sm_in[4 * tid + 1] = make_uint4(c.g[4], c.g[5], c.g[6], c.g[7]);
-            sm_in[4 * tid + 2] = make_uint4(c.mq[0], c.mq[1], c.mq[2], c.mq[3]);
-            sm_in[4 * tid + 3] = make_uint4(c.vq[0], c.vq[1], c.vq[2], c.vq[3]);
-        }
 
         // smallest non-zero values as keys; a lane holding an exact zero (rare:
         // both inputs of an element zero, or a fast sum that cancels) rescans
@@ -759,17 +745,9 @@ step_kernel_cta(const StepArgs a) {
             h &= h - 1u;
             const int th = (int)R.hwarp(ri) * 32 + ln;
             float* vals = second ? sm_v[th] : sm_m[th];
-            // the holder's gradients and codes (zero beyond n)
+            // the holder's gradients and codes, read again from L2 (zero beyond n)
             uint32_t gw[8], cw[4];
-            if constexpr (Lay::kStash) {
-                const uint4 g0 = sm_in[4 * th], g1 = sm_in[4 * th + 1];
-                const uint4 cc = sm_in[4 * th + (second ? 3 : 2)];
-                gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
-                gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
-                cw[0] = cc.x; cw[1] = cc.y; cw[2] = cc.z; cw[3] = cc.w;
-            } else {
-                reload_inputs(a, cta_base + (int64_t)th * kVec, second, gw, cw);
-            }
+            reload_inputs(a, cta_base + (int64_t)th * kVec, second, gw, cw);
             uint32_t msk = 0u;
             if constexpr (kStatBlocks) {
                 // the window test of the job's statistic alone (`cand` without its
