@@ -113,8 +113,8 @@ __device__ __forceinline__ void load_chunk(const StepArgs& a, int64_t base, bool
         const uint4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
         c.g[0] = g0.x; c.g[1] = g0.y; c.g[2] = g0.z; c.g[3] = g0.w;
         c.g[4] = g1.x; c.g[5] = g1.y; c.g[6] = g1.z; c.g[7] = g1.w;
-        const uint4 m = __ldcg(reinterpret_cast<const uint4*>(a.mq + base));
-        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.vq + base));
+        const uint4 m = __ldg(reinterpret_cast<const uint4*>(a.mq + base));
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.vq + base));
         c.mq[0] = m.x; c.mq[1] = m.y; c.mq[2] = m.z; c.mq[3] = m.w;
         c.vq[0] = v.x; c.vq[1] = v.y; c.vq[2] = v.z; c.vq[3] = v.w;
     } else {
@@ -143,7 +143,7 @@ __device__ __forceinline__ void reload_inputs(const StepArgs& a, int64_t b, bool
     if (b + kVec <= a.n) {
         const uint4* gp = reinterpret_cast<const uint4*>(a.g + b);
         const uint4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
-        const uint4 cc = __ldcg(reinterpret_cast<const uint4*>(q + b));
+        const uint4 cc = __ldg(reinterpret_cast<const uint4*>(q + b));
         gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
         gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
         cw[0] = cc.x; cw[1] = cc.y; cw[2] = cc.z; cw[3] = cc.w;
