@@ -21,42 +21,24 @@ struct Geom {
     static constexpr int kGpc = kJobs ? kThreads * kVec / G : 1;   // groups per CTA
 };
 
-// Eight 256-thread CTAs per SM for G >= 16 (32 registers, a few spilled):
-// with one group per thread the kernels are latency-bound and occupancy pays
-// more than the spills cost; below G = 16 a thread holds 16/G groups and the
-// register need grows with them.
+// The per-group shared arrays of the job form (G >= 32).
+template <int N>
+struct QuantJobs {
+    float mx[N], k[N], inv[N], pre[N];
+    uint32_t mn[N];
+};
+
+// One thread's 16 values x of the tile starting at element `base`: group
+// statistics, k and S (formed once per group of the CTA in the job form),
+// codes stored, and the group records written.  Every thread of the CTA
+// calls it (the job form has CTA barriers).
 template <int G>
-__global__ void __launch_bounds__(kThreads, G >= kVec ? 8 : 1)
-dre_quantize_kernel(const QuantArgs a) {
+__device__ __forceinline__ void quantize_tile(const QuantArgs& a, const float (&x)[kVec], int64_t base,
+                                              int64_t cta_group0, const df::Tables& tab,
+                                              QuantJobs<Geom<G>::kGpc>& sj) {
     using Gm = Geom<G>;
-    __shared__ SmemTables st;
-    __shared__ float s_mx[Gm::kGpc], s_k[Gm::kGpc], s_inv[Gm::kGpc], s_pre[Gm::kGpc];
-    __shared__ uint32_t s_mn[Gm::kGpc];
-    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const int64_t base = tid * kVec;
-    // the table fill's barrier below and the job phase's barriers: only the
-    // per-lane form, which has no job phase, may leave before them
     const bool active = base < a.n;
     const bool full = base + kVec <= a.n;
-
-    // the inputs first: their loads are in flight while the tables are filled
-    float x[kVec];
-    if (active && full) {
-        const float4* xp = reinterpret_cast<const float4*>(a.x + base);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float4 t = ld_cs(xp + i);
-            x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
-        }
-    } else {
-#pragma unroll
-        for (int e = 0; e < kVec; ++e) x[e] = (active && base + e < a.n) ? a.x[base + e] : 0.0f;
-    }
-    load_smem_tables(st, threadIdx.x, kThreads);
-    __syncthreads();
-    const df::Tables tab = tables_of(st);
-    if (!Gm::kJobs && __all_sync(0xFFFFFFFFu, base >= a.n)) return;
-
     float mx[Gm::kGroups];
     uint32_t mn[Gm::kGroups];
 #pragma unroll
@@ -80,31 +62,30 @@ dre_quantize_kernel(const QuantArgs a) {
         // constants (the lanes of a group would otherwise each repeat them)
         const int gl = (int)((threadIdx.x * kVec) / G);
         if ((threadIdx.x * kVec) % G == 0) {
-            s_mx[gl] = mx[0];
-            s_mn[gl] = mn[0];
+            sj.mx[gl] = mx[0];
+            sj.mn[gl] = mn[0];
         }
         __syncthreads();
-        const int64_t gcta = (int64_t)blockIdx.x * Gm::kGpc;
         for (int j = threadIdx.x; j < Gm::kGpc; j += kThreads) {
-            const float gm = s_mx[j];
-            QuantParams q = quant_params_precise(gm, nz_key_value(s_mn[j]), tab);
+            const float gm = sj.mx[j];
+            QuantParams q = quant_params_precise(gm, nz_key_value(sj.mn[j]), tab);
             float pr = 1.0f;
             if (gm > 0.0f && gm < 1.17549435e-38f) {
                 pr = 16777216.0f;
                 q.inv_mx = __frcp_rn(gm * 16777216.0f);
             }
-            s_k[j] = q.k;
-            s_inv[j] = q.inv_mx;
-            s_pre[j] = pr;
-            if ((gcta + j) * G < a.n) {
-                a.scale[gcta + j] = q.S;
-                a.k[gcta + j] = q.k;
+            sj.k[j] = q.k;
+            sj.inv[j] = q.inv_mx;
+            sj.pre[j] = pr;
+            if ((cta_group0 + j) * G < a.n) {
+                a.scale[cta_group0 + j] = q.S;
+                a.k[cta_group0 + j] = q.k;
             }
         }
         __syncthreads();
-        qp[0].k = s_k[gl];
-        qp[0].inv_mx = s_inv[gl];
-        pre[0] = s_pre[gl];
+        qp[0].k = sj.k[gl];
+        qp[0].inv_mx = sj.inv[gl];
+        pre[0] = sj.pre[gl];
     } else {
 #pragma unroll
         for (int j = 0; j < Gm::kGroups; ++j) {
@@ -145,6 +126,35 @@ dre_quantize_kernel(const QuantArgs a) {
                 if ((g0 + j) * G < a.n) { a.scale[g0 + j] = qp[j].S; a.k[g0 + j] = qp[j].k; }
         }
     }
+}
+
+// One tile of 4096 elements per CTA.  Eight 256-thread CTAs per SM for
+// G >= 16 (32 registers, a few spilled): the kernel is latency-bound and
+// occupancy pays more than the spills cost; below G = 16 a thread holds 16/G
+// groups and the register need grows with them.
+template <int G>
+__global__ void __launch_bounds__(kThreads, G >= kVec ? 8 : 1)
+dre_quantize_kernel(const QuantArgs a) {
+    __shared__ SmemTables st;
+    __shared__ QuantJobs<Geom<G>::kGpc> sj;
+    const int64_t base = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * kVec;
+    // the inputs first: their loads are in flight while the tables are filled
+    float x[kVec];
+    if (base + kVec <= a.n) {
+        const float4* xp = reinterpret_cast<const float4*>(a.x + base);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 t = ld_cs(xp + i);
+            x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) x[e] = base + e < a.n ? a.x[base + e] : 0.0f;
+    }
+    load_smem_tables(st, threadIdx.x, kThreads);
+    __syncthreads();
+    if (!Geom<G>::kJobs && __all_sync(0xFFFFFFFFu, base >= a.n)) return;
+    quantize_tile<G>(a, x, base, (int64_t)blockIdx.x * Geom<G>::kGpc, tables_of(st), sj);
 }
 
 // Per-group parameters of the dequantizer: 2^z with z = log2(448 S) / k split

@@ -72,6 +72,29 @@ def test_quantize_matches_oracle(G):
     print(G, st)
 
 
+@pytest.mark.parametrize("G", [32, 128, 256])
+def test_quantize_several_tiles_per_cta(G):
+    """A buffer of more than three tiles of 4096 elements for each of eight
+    CTAs per SM, with a ragged last tile and a few all-zero and one-non-zero
+    groups: the quantizer's persistent form (G >= 32) takes several tiles per
+    CTA; codes, S and k against the oracle over the whole buffer."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = 3 * 8 * sms * 4096 + 5 * G + G // 2 + 7
+    ng = (n + G - 1) // G
+    rng = np.random.default_rng(300 + G)
+    s = 10.0 ** rng.uniform(-12, 2, ng)
+    x = (rng.standard_normal(ng * G) * np.repeat(s, G))[:n].astype(np.float32)
+    x[:4 * G] = 0.0
+    x[4 * G + 3] = 1.5
+    x[5 * G:6 * G] = 0.0
+    x[6 * G] = -2.0e-30
+    qg, Sg, kg = gpu_quantize(x, G)
+    qo, So, ko = oracle.dre_quantize(x, G)
+    st = P.compare_codes(qg, qo, f"many tiles G={G}")
+    st.update(P.compare_meta(Sg, kg, So, ko, f"many tiles G={G}", state_rel=0.0))
+    print(G, st)
+
+
 # The dequantizer's bar: within 1e-6 relative of the oracle's correctly
 # rounded fp32 value (the bar of the step's weights, scales and exponents),
 # or one fp32 subnormal step for results below 2^-126, which are scaled with a
