@@ -60,8 +60,7 @@ __device__ unsigned long long g_recompute[2];
 // read them, so the step kernel's shared memory holds that path's inputs
 // instead.
 __device__ __forceinline__ df::Tables global_tables() {
-    return df::Tables{reinterpret_cast<const float*>(gtab::kLog2CenterHi),
-                      reinterpret_cast<const float*>(gtab::kLog2CenterLo),
+    return df::Tables{reinterpret_cast<const df::LogEntry*>(gtab::kLog2Recip),
                       reinterpret_cast<const float*>(gtab::kExp2FracHi),
                       reinterpret_cast<const float*>(gtab::kExp2FracLo)};
 }

@@ -137,15 +137,13 @@ struct QuantParams {
 // Shared-memory copy of the double-float tables (divergent indices: constant
 // memory would serialize them).
 struct SmemTables {
-    float log2c_hi[64], log2c_lo[64];
+    df::LogEntry logr[256];
     float exp2j_hi[33], exp2j_lo[33];
 };
 
 __device__ __forceinline__ void load_smem_tables(SmemTables& st, int tid, int nthreads) {
-    for (int i = tid; i < 64; i += nthreads) {
-        st.log2c_hi[i] = __uint_as_float(gtab::kLog2CenterHi[i]);
-        st.log2c_lo[i] = __uint_as_float(gtab::kLog2CenterLo[i]);
-    }
+    const uint2* src = reinterpret_cast<const uint2*>(gtab::kLog2Recip);
+    for (int i = tid; i < 256; i += nthreads) reinterpret_cast<uint2*>(st.logr)[i] = src[i];
     for (int i = tid; i < 33; i += nthreads) {
         st.exp2j_hi[i] = __uint_as_float(gtab::kExp2FracHi[i]);
         st.exp2j_lo[i] = __uint_as_float(gtab::kExp2FracLo[i]);
@@ -153,7 +151,7 @@ __device__ __forceinline__ void load_smem_tables(SmemTables& st, int tid, int nt
 }
 
 __device__ __forceinline__ df::Tables tables_of(const SmemTables& st) {
-    return df::Tables{st.log2c_hi, st.log2c_lo, st.exp2j_hi, st.exp2j_lo};
+    return df::Tables{st.logr, st.exp2j_hi, st.exp2j_lo};
 }
 
 __device__ __forceinline__ df::F2 const_df(const unsigned int* p) {

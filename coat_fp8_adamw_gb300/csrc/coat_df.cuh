@@ -8,10 +8,12 @@
 // fused multiply-add and divide with round-to-nearest-even -- so the same
 // code gives bit-identical results on the device and on the host (where the
 // CPU tests exercise it).  The error-free transformations are Knuth's
-// TwoSum, Dekker's FastTwoSum and the FMA-based TwoProduct; log2 uses a
-// 64-entry table of log2(c_j) with the atanh series of ln(u/c_j); exp2 uses a
-// 32-entry table of 2^(j/32) with the Taylor series of e^a on |a| < 0.011.
-// The tables are generated in float64 by gen_tables.py.
+// TwoSum, Dekker's FastTwoSum and the FMA-based TwoProduct; log2 reduces the
+// significand u by a 9-bit reciprocal r_j of its interval (one of 256; then
+// u r_j - 1 is exact in fp32, one FMA) and sums -log2 r_j (a 256-entry table)
+// with the Taylor series of log2(1 + t) on |t| < 2^-8.45; exp2 uses a 32-entry table of
+// 2^(j/32) with the Taylor series of e^a on |a| < 0.011.  The tables are
+// generated in float64 by gen_tables.py.
 #pragma once
 
 #include <cstdint>
@@ -155,9 +157,12 @@ COAT_HD float div22_rn(F2 a, F2 b) {
 }
 
 // --- constants (double-float) ---
+// One entry of the log2 reduction table: -log2 r_j (double-float).
+struct alignas(8) LogEntry {
+    float nl_hi, nl_lo;
+};
 struct Tables {
-    const float* log2c_hi;  // [64] log2(1 + (2j+1)/128)
-    const float* log2c_lo;
+    const LogEntry* logr;   // [256], interval j of the significand (top 8 bits)
     const float* exp2j_hi;  // [33] 2^(j/32), j = -16..16 (index j + 16)
     const float* exp2j_lo;
 };
@@ -166,7 +171,35 @@ constexpr float kInvLn2Lo = 1.925963033500011079013347625732421875e-08f;
 constexpr float kLn2Hi = 0.693147182464599609375f;           // ln 2 = hi + lo
 constexpr float kLn2Lo = -1.9046542121259336e-09f;
 
-// log2(x) for finite x > 0 (normal or subnormal), |error| <~ 2^-46 + 2^-47 |log2 x|.
+// The Taylor coefficients of log2(1 + t) beyond the quadratic term, as floats:
+// 1/(3 ln 2), -1/(4 ln 2), 1/(5 ln 2).
+constexpr float kL2c3 = 0.480898350f;
+constexpr float kL2c4 = -0.360673755f;
+constexpr float kL2c5 = 0.288539022f;
+
+// The reciprocal of the log2 reduction for interval j = 0..255 of the
+// significand: r_j = rint(p(j)) / 512 with p a quartic close to
+// 2^18 / (513 + 2j) (within 0.11), evaluated by FMAs, so r_j is a 9-bit value
+// near 1 / (interval centre) with |u r_j - 1| < 2^-8.38 for every u in
+// [1 + j/256, 1 + (j+1)/256); gen_tables.py reads the coefficients from here,
+// repeats the evaluation exactly, checks that bound and tabulates -log2 r_j.
+constexpr float kRecipP4 = 0x1.4a7454p-26f;
+constexpr float kRecipP3 = -0x1.197b28p-16f;
+constexpr float kRecipP2 = 0x1.bf7b12p-8f;
+constexpr float kRecipP1 = -0x1.f7a158p+0f;
+constexpr float kRecipP0 = 0x1.fee4eep+8f;
+COAT_HD float log_recip(uint32_t j) {
+    const float x = (float)j;
+    const float p = fma(fma(fma(fma(kRecipP4, x, kRecipP3), x, kRecipP2), x, kRecipP1), x, kRecipP0);
+    return mul(rint(p), 0.001953125f);
+}
+
+// log2(x) for finite x > 0 (normal or subnormal), |error| < 2^-46 + 2^-47 |log2 x|.
+// x = 2^e u, u in [1, 2); with the table's r_j for the top 8 bits of u,
+// t = u r_j - 1 is exact (|t| < 2^-8.38) and
+//   log2 x = e - log2 r_j + c t - (c/2) t^2 + t^3 (c/3 - c t/4 + c t^2/5),
+// c = 1/ln 2, truncated after t^5 (the next term is below 2^-52).  c t and
+// (c/2) t^2 are carried as double-floats; the cubic tail (< 2^-26.2) in fp32.
 COAT_HD F2 log2_df(float x, const Tables& t) {
     uint32_t b = bits(x);
     int ex = (int)((b >> 23) & 0xFFu);
@@ -174,26 +207,22 @@ COAT_HD F2 log2_df(float x, const Tables& t) {
         b = bits(mul(x, 16777216.0f));
         ex = (int)((b >> 23) & 0xFFu) - 24;
     }
-    const int e = ex - 127;
-    const uint32_t j = (b >> 17) & 63u;
+    const uint32_t j = (b >> 15) & 255u;
+    const LogEntry en = t.logr[j];
     const float u = from_bits((b & 0x007FFFFFu) | 0x3F800000u);
-    const float c = from_bits(0x3F800000u | (j << 17) | (1u << 16));  // 1 + (2j+1)/128
-    // s = (u - c) / (u + c), |s| <= 2^-8
-    const float num = sub(u, c);                 // exact (Sterbenz)
-    const F2 den = fast_two_sum(u, c);           // same binade: exact split
-    const float s = div(num, den.hi);
-    const float r = fma(-s, den.lo, fma(-s, den.hi, num));
-    const float s_lo = div(r, den.hi);
-    // ln(u/c) = 2 atanh(s) = 2s + (2/3)s^3 + (2/5)s^5 + O(s^7)
-    const float s2 = mul(s, s);
-    const float poly = mul(mul(s, s2), fma(0.4f, s2, 0.666666686534881591796875f));
-    const F2 ln_uc = fast_two_sum(mul(2.0f, s), add(mul(2.0f, s_lo), poly));
-    // to base 2
-    const F2 l2 = mul22(ln_uc, F2{kInvLn2Hi, kInvLn2Lo});
-    // + log2(c_j) + e
-    const F2 lc = {t.log2c_hi[j], t.log2c_lo[j]};
-    const F2 frac = add2(lc, l2);                  // in [0, 1)
-    const F2 whole = two_sum((float)e, frac.hi);
+    const float w = fma(u, log_recip(j), -1.0f);          // t, exact
+    const F2 a = two_prod(w, kInvLn2Hi);                  // c_hi t
+    const F2 sq = two_prod(w, w);                         // t^2
+    const F2 q = two_prod(sq.hi, mul(0.5f, kInvLn2Hi));   // (c_hi / 2) (t^2).hi
+    const float tail = mul(mul(w, sq.hi), fma(fma(w, kL2c5, kL2c4), w, kL2c3));
+    // the small parts: the low halves of the two products, c_lo t, the tail,
+    // (c_hi / 2) (t^2).lo and (c_lo / 2) t^2
+    const float small = add(add(sub(a.lo, q.lo), fma(w, kInvLn2Lo, tail)),
+                            -fma(mul(0.5f, kInvLn2Hi), sq.lo, mul(mul(0.5f, kInvLn2Lo), sq.hi)));
+    const F2 l1 = fast_two_sum(a.hi, -q.hi);              // |q.hi| < |a.hi| / 256
+    const F2 lt = fast_two_sum(l1.hi, add(l1.lo, small)); // log2(1 + t)
+    const F2 frac = add2(F2{en.nl_hi, en.nl_lo}, lt);      // log2 u, in [0, 1)
+    const F2 whole = two_sum((float)(ex - 127), frac.hi);
     return two_sum(whole.hi, add(whole.lo, frac.lo));
 }
 

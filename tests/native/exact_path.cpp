@@ -29,10 +29,11 @@ static float e4m3_mag(unsigned mag) {
 }
 
 int main() {
-    float lc_hi[64], lc_lo[64], e_hi[33], e_lo[33];
-    for (int i = 0; i < 64; ++i) { lc_hi[i] = u2f(kLog2CenterHi[i]); lc_lo[i] = u2f(kLog2CenterLo[i]); }
+    static coat::df::LogEntry logr[256];
+    float e_hi[33], e_lo[33];
+    std::memcpy(logr, kLog2Recip, sizeof(logr));
     for (int i = 0; i < 33; ++i) { e_hi[i] = u2f(kExp2FracHi[i]); e_lo[i] = u2f(kExp2FracLo[i]); }
-    const coat::df::Tables t{lc_hi, lc_lo, e_hi, e_lo};
+    const coat::df::Tables t{logr, e_hi, e_lo};
     const coat::df::KConsts kc{cdf(kLog2RDf), cdf(kGuardLoDf), cdf(kGuardHiDf), 8.0f,
                                448.0 * 512.0, -125.0, 126.0};
     char kind[4];
