@@ -550,11 +550,15 @@ step_kernel_cta(const StepArgs a) {
     // Bulk L2 prefetch of the tile of the CTA kL2Ahead launches later (roughly
     // half a wave on GB300): its DRAM reads start while this CTA computes, so
     // more requests are in flight than the CTAs' own loads keep (3.7 % off the
-    // Llama-2-7B step).  One thread, four bulk prefetches; a tile that ends
-    // past n is not prefetched.
+    // Llama-2-7B step).  One thread, four bulk prefetches, and for G <= 32 a
+    // fifth for the group records (phase B reads them first and every warp
+    // waits for B: 2.7 % off the step at G = 16 and 32; no gain at G = 64, and
+    // at G = 128 the 256 bytes are not worth the extra request); a tile that
+    // ends past n is not prefetched.
     {
         const int64_t pf = cta_base + (int64_t)kL2Ahead * kCtaElems;
         if (tid == 0 && pf + kCtaElems <= a.n) {
+            if constexpr (G <= 32) l2_prefetch(a.meta + pf / G, NGC * 16);
             l2_prefetch(a.w + pf, kCtaElems * 4);
             l2_prefetch(a.g + pf, kCtaElems * 2);
             l2_prefetch(a.mq + pf, kCtaElems);
