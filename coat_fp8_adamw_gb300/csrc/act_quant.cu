@@ -15,9 +15,9 @@
 // per thread and pass, statistics per thread and then across the G/8 lanes of
 // a group), store q and the scales, stage the codes in shared memory, and then
 // write qt as 16-byte runs of one column, each built from 4 x 4 byte
-// transposes.  A thread keeps four passes' loads in flight at a time, which
-// holds it to 48 registers: ten CTAs per SM hide more latency than eight
-// passes of loads in flight in fewer CTAs.
+// transposes.  The tile's inputs are copied into shared memory (cp.async) all
+// at once when the CTA starts, so that its eight passes cost one memory
+// latency without holding registers for the loads in flight.
 #include <cstdint>
 
 #include "coat_device.cuh"
@@ -39,15 +39,26 @@ __device__ __forceinline__ float div448_bf16(float m) {
 }
 
 
+// 16-byte asynchronous copy global -> shared (L2 only, no L1 allocation), and
+// the wait for all of this thread's copies.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_all;" ::: "memory");
+}
+
 constexpr int kTileR = 64;                  // rows per tile
 constexpr int kTileC = 128;                 // columns per tile
 constexpr int kActThreads = 128;
 constexpr int kPitchW = kTileC / 4 + 1;     // shared-memory row pitch in words (padded)
 
 template <int G>
-__global__ void __launch_bounds__(kActThreads, 10)
+__global__ void __launch_bounds__(kActThreads, 9)
 act_quant_kernel(const ActArgs a) {
     __shared__ uint32_t tile[kTileR * kPitchW];
+    __shared__ uint4 stage[kTileR / 8][kActThreads];   // the tile's inputs, [pass][thread]
     const int tid = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.y * kTileR;
     const int64_t col0 = (int64_t)blockIdx.x * kTileC;
@@ -57,19 +68,20 @@ act_quant_kernel(const ActArgs a) {
     const int r_in = tid >> 4;              // row within the pass
     const int c8 = (tid & 15) * 8;          // first column of this thread
     const bool col_ok = col0 + c8 < a.N;    // N % 16 == 0: all 8 columns or none
-    uint4 raw[kTileR / 16];
+    // every pass's 16 bytes copied into shared memory at once (no registers
+    // held while they are in flight); a thread reads back only its own slots,
+    // so waiting for its own copies is enough
 #pragma unroll
     for (int p = 0; p < kTileR / 8; ++p) {
-        if ((p & 3) == 0) {   // four passes' loads in flight at a time
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const int64_t rr = row0 + 8 * (p + h) + r_in;
-                raw[h] = make_uint4(0u, 0u, 0u, 0u);
-                if (rr < a.M && col_ok) raw[h] = ld_cs(reinterpret_cast<const uint4*>(a.x + rr * a.N + col0 + c8));
-            }
-        }
+        const int64_t rr = row0 + 8 * p + r_in;
+        if (rr < a.M && col_ok) cp_async16(&stage[p][tid], a.x + rr * a.N + col0 + c8);
+    }
+    cp_async_wait_all();
+#pragma unroll 1
+    for (int p = 0; p < kTileR / 8; ++p) {
         const int64_t r = row0 + 8 * p + r_in;
-        const uint32_t w[4] = {raw[p & 3].x, raw[p & 3].y, raw[p & 3].z, raw[p & 3].w};
+        const uint4 v = (r < a.M && col_ok) ? stage[p][tid] : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         float x[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -109,13 +121,27 @@ act_quant_kernel(const ActArgs a) {
             codes[e / 4] |= clo << (16 * ((e >> 1) & 1));
             diff[e / 4] |= (clo ^ chi) << (16 * ((e >> 1) & 1));
         }
-        if ((diff[0] | diff[1]) != 0u || inv_bad) {   // rare: quotients beside a midpoint
+        if (inv_bad) {   // a subnormal scale: every element by division
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int sh = 8 * (e & 3);
-                if (((diff[e / 4] >> sh) & 0xFFu) != 0u || !(inv[e / kPer] <= 3.40282347e38f)) {
-                    const uint32_t c = S[e / kPer] > 0.0f ? e4m3_code_of_quotient_exact(x[e], S[e / kPer]) : 0u;
+                if (!(inv[e / kPer] <= 3.40282347e38f)) {
+                    const uint32_t c = e4m3_code_of_quotient_exact(x[e], S[e / kPer]);
                     codes[e / 4] = (codes[e / 4] & ~(0xFFu << sh)) | (c << sh);
+                    diff[e / 4] &= ~(0xFFu << sh);
+                }
+            }
+        }
+        if ((diff[0] | diff[1]) != 0u) {   // quotients beside a midpoint: the midpoint decides
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int wd = i >> 1, sh = 16 * (i & 1);
+                const uint32_t d = (diff[wd] >> sh) & 0xFFFFu;
+                if (d != 0u) {
+                    const uint32_t lo = (codes[wd] >> sh) & 0xFFFFu;
+                    const uint32_t c = e4m3x2_resolve(lo, lo ^ d, x[2 * i], x[2 * i + 1], S[(2 * i) / kPer],
+                                                      S[(2 * i + 1) / kPer]);
+                    codes[wd] = (codes[wd] & ~(0xFFFFu << sh)) | (c << sh);
                 }
             }
         }

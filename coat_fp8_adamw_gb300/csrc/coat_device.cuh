@@ -204,14 +204,20 @@ __device__ __forceinline__ float expand_scaled(float x, float r, float k) {
 // quotient (midpoints are floats, and the quotient is within half a float step
 // of y), so this only matters when y is a midpoint.  Midpoints: 4 significant
 // bits with the 4th set for |y| >= 2^-6, odd multiples of 2^-10 below.  S > 0.
+// The remainder is exact only while it stays above the fp32 subnormal range:
+// near a midpoint (>= 2^-10) of a quotient of an x below 2^-100 it can be
+// about 2^-154 and round to zero, so such x and S are first scaled by 2^64
+// (exact; the quotient is unchanged).
 __device__ __forceinline__ float e4m3_quotient(float x, float S) {
-    const float y = __fdiv_rn(x, S);
+    const float k = fabsf(x) < 0x1p-100f ? 0x1p64f : 1.0f;
+    const float xs = x * k, Ss = S * k;
+    const float y = __fdiv_rn(xs, Ss);
     const float ay = fabsf(y);
     const uint32_t b = __float_as_uint(ay);
     const float t = ay * 1024.0f;
     const bool mid = ay >= 0.015625f ? (b & 0xFFFFFu) == 0x80000u
                                      : (t == rintf(t) && (((uint32_t)t) & 1u) != 0u);
-    const float r = fmaf(-y, S, x);
+    const float r = fmaf(-y, Ss, xs);
     if (!mid || r == 0.0f) return y;
     return __uint_as_float(__float_as_uint(y) + (((r > 0.0f) == (y > 0.0f)) ? 1u : 0xFFFFFFFFu));
 }
@@ -235,6 +241,36 @@ __device__ __forceinline__ uint32_t e4m3_code_fast(float x, float inv, bool& und
 // The rare case, out of line so that it stays a branch taken by few lanes.
 static __device__ __noinline__ uint32_t e4m3_code_of_quotient_exact(float x, float S) {
     return e4m3x2(__fadd_rn(e4m3_quotient(x, S), 0.0f), 0.0f) & 0xFFu;
+}
+
+// The exact codes of a pair of elements x0, x1 (scales S0, S1 > 0, normal)
+// whose probe codes lo (of y (1 - 2^-20)) and hi (of y (1 + 2^-20)) may differ,
+// 16 bits each.  The exact quotient x / S lies between the two probes, so its
+// correctly rounded code is lo or hi, adjacent codes, and the midpoint
+// between their values decides: the sign of 2|x| - (|lo| + |hi|) S, formed by
+// one FMA (the sum is exact, and the FMA's rounding keeps the sign), says on
+// which side the quotient lies; zero is a tie, which goes to the even code.
+// A byte where lo and hi agree keeps its code.  The FMA could round a non-zero
+// difference to zero only if it fell below 2^-149: its operands are multiples
+// of 2^-142 or coarser unless |x| < 2^-100, and such an x (with S below 2^-89,
+// as x / S is near a midpoint, at least 2^-11) is scaled with S by 2^64 first
+// (exact).
+__device__ __forceinline__ uint32_t e4m3x2_resolve(uint32_t lo, uint32_t hi, float x0, float x1, float S0,
+                                                   float S1) {
+    uint32_t hl, hh, hs;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hl) : "h"((unsigned short)(lo & 0x7F7Fu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"((unsigned short)(hi & 0x7F7Fu)));
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(hs) : "r"(hl), "r"(hh));   // exact: 5 significant bits
+    float s0, s1;
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(s0), "=f"(s1) : "r"(hs));
+    const float a0 = fabsf(x0), a1 = fabsf(x1);
+    const float k0 = a0 < 0x1p-100f ? 0x1p64f : 1.0f, k1 = a1 < 0x1p-100f ? 0x1p64f : 1.0f;
+    float r0, r1;
+    upk(fma2(pk(-s0, -s1), mul2(pk(S0, S1), pk(k0, k1)), mul2(pk(a0, a1), pk(2.0f * k0, 2.0f * k1))), r0, r1);
+    const bool up0 = r0 > 0.0f || (r0 == 0.0f && (lo & 1u) != 0u);
+    const bool up1 = r1 > 0.0f || (r1 == 0.0f && (lo & 0x100u) != 0u);
+    return ((up0 ? hi : lo) & 0xFFu) | ((up1 ? hi : lo) & 0xFF00u);
 }
 
 // The stored code of a zero is 0x00 whatever the sign of the value that

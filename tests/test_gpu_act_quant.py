@@ -109,13 +109,18 @@ def _midpoint_groups():
     return np.array(groups, np.float32)
 
 
-def test_quotients_beside_a_midpoint_round_like_the_exact_quotient():
-    """Both quantizers must round the exact quotient, not its float32 rounding."""
+@pytest.mark.parametrize("scale", [1.0, -(2.0 ** -112)])
+def test_quotients_beside_a_midpoint_round_like_the_exact_quotient(scale):
+    """Both quantizers must round the exact quotient, not its float32 rounding;
+    also for negative values around 2^-120, where the activation quantizer
+    scales the midpoint test into range."""
     G = 4
-    grp = _midpoint_groups()
+    grp = _midpoint_groups() * np.float32(scale)
+    back = (synth.f32_to_bf16_bits(grp).astype(np.uint32) << 16).view(np.float32).reshape(grp.shape)
+    grp = grp[np.all(back == grp, axis=1)]              # every value still exact in bf16
     grp = grp[: (len(grp) // 64) * 64]                  # rows of 16 elements, M a multiple of 16
     x = grp.reshape(-1, 16)
-    S32 = (x[:, ::4].astype(np.float64) / 448).astype(np.float32)
+    S32 = (np.abs(x[:, ::4]).astype(np.float64) / 448).astype(np.float32)
     naive = torch.from_numpy((x[:, 1::4] / S32).astype(np.float32)).to(torch.float8_e4m3fn)
     qo, _, So = oracle.act_quantize(synth.f32_to_bf16_bits(x).reshape(x.shape), G)
     disagree = (naive.view(torch.uint8).numpy() != qo[:, 1::4]).sum()
