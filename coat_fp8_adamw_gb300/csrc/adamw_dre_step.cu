@@ -215,7 +215,7 @@ struct StateParams {
 __device__ __forceinline__ StateParams state_params(float S, float k, const df::Tables& t) {
     StateParams p;
     p.S = S;
-    p.rkd = df::div21(F2{1.0f, 0.0f}, k);
+    p.rkd = df::recip21(k);
     if (S > 0.0f) {
         p.A = df::add2(df::log2_df(S, t), const_df(kLog2_448Df));
         const F2 z = df::mul22(p.A, p.rkd);                 // log2 P

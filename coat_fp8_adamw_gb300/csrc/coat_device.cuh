@@ -161,8 +161,9 @@ __device__ __forceinline__ df::F2 const_df(const unsigned int* p) {
 // The exponent rule's constants (R_E4M3 = 448 / 2^-9, cap 8, S kept in
 // [2^-125, 2^126]) for df::k_certain.
 __device__ __forceinline__ df::KConsts k_consts() {
-    return df::KConsts{const_df(kLog2RDf), const_df(kGuardLoDf), const_df(kGuardHiDf), kKCap,
-                       448.0 * 512.0, -125.0, 126.0};
+    return df::KConsts{const_df(kLog2RDf), const_df(kGuardLoDf), const_df(kGuardHiDf),
+                       __uint_as_float(kLog2RRcp), __uint_as_float(kGuardLoRcp), __uint_as_float(kGuardHiRcp),
+                       kKCap, 448.0 * 512.0, -125.0, 126.0};
 }
 
 // Fresh per-group parameters with k correctly rounded to fp32 (double-float

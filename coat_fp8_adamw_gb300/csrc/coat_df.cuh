@@ -144,6 +144,22 @@ COAT_HD F2 div21(F2 a, float b) {
     const float r = add(fma(-q, b, a.hi), a.lo);  // a.hi - q b is exact for a rounded quotient
     return fast_two_sum(q, div(r, b));
 }
+// 1 / b as a double-float with one division: q = RN(1/b), the exact remainder
+// 1 - q b (one FMA), and its quotient by b formed as a product with q (a
+// relative error of 2^-23 on a part below 2^-24 q).
+COAT_HD F2 recip21(float b) {
+    const float q = div(1.0f, b);
+    const float r = fma(-q, b, 1.0f);
+    return fast_two_sum(q, mul(r, q));
+}
+// a / b for two double-floats as an unrounded pair q + c, with 1 / a.hi given
+// (a constant numerator): the correction r / b.hi is formed as r q (1 / a.hi),
+// within a relative 2^-22 of it; |c| <= ulp(q).
+COAT_HD F2 div22_parts_k(F2 a, float rcp_a_hi, F2 b) {
+    const float q = div(a.hi, b.hi);
+    const float r = sub(add(fma(-q, b.hi, a.hi), a.lo), mul(q, b.lo));
+    return {q, mul(r, mul(q, rcp_a_hi))};
+}
 // a / b for two double-floats as an unrounded pair q + c (|c| <= ulp(q))
 COAT_HD F2 div22_parts(F2 a, F2 b) {
     const float q = div(a.hi, b.hi);

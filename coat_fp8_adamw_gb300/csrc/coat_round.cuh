@@ -50,6 +50,25 @@ COAT_HD float round_certain(F2 v, float eps, bool& certain) {
     certain = d > mul(eps, abs1(r));
     return r;
 }
+// The same test with the relative error bound given as num / den (den > 0):
+// d > (num / den) |r| taken as d den > num |r|, without the division (the two
+// products' roundings move the bound by a relative 2^-23, far inside its
+// margin).
+COAT_HD float round_certain_q(F2 v, float num, float den, bool& certain) {
+    const F2 s = fast_two_sum(v.hi, v.lo);
+    const float r = s.hi;
+    if (r == 0.0f) {
+        certain = v.lo == 0.0f;
+        return r;
+    }
+    const uint32_t b = bits(r);
+    const bool outward = (s.lo > 0.0f) == (r > 0.0f);
+    const float nb = from_bits(outward ? b + 1u : b - 1u);
+    const float half = mul(0.5f, abs1(sub(nb, r)));
+    const float d = sub(half, abs1(s.lo));
+    certain = mul(d, den) > mul(num, abs1(r));
+    return r;
+}
 
 // The dequantized moment sign-free: (|E4M3(q)| S)^(1/k) in float64, rounded
 // once to fp32 (the definition, for the values the double-float path cannot
@@ -91,8 +110,11 @@ COAT_HD_OUTLINE float k_f64(float mx, float mn, double R, double cap, double s_l
 COAT_HD float dequant_err_bound(float z_abs, float A_abs, float rk) {
     return mul(0x1p-42f, add(add(z_abs, mul(A_abs, rk)), 1.0f));
 }
+COAT_HD float k_err_num(float lmx_abs, float lmn_abs) {
+    return mul(0x1p-43f, add(add(2.0f, lmx_abs), lmn_abs));
+}
 COAT_HD float k_err_bound(float lmx_abs, float lmn_abs, float d_abs) {
-    return div(mul(0x1p-43f, add(add(2.0f, lmx_abs), lmn_abs)), d_abs);
+    return div(k_err_num(lmx_abs, lmn_abs), d_abs);
 }
 
 // Correctly rounded fp32 magnitude of a dequantized moment
@@ -124,6 +146,7 @@ COAT_HD float dequant_certain(F2 L, F2 A, F2 rkd, float mag, float S, float k, c
 // for the float64 recomputation.
 struct KConsts {
     F2 log2R, guard_lo, guard_hi;
+    float rcp_log2R, rcp_guard_lo, rcp_guard_hi;   // 1 / the high parts
     float cap;
     double R, s_lo, s_hi;
 };
@@ -140,16 +163,17 @@ COAT_HD float k_certain(float mx, float mn, F2 Lmx, F2 Lmn, const KConsts& c, bo
     if (mn > 0.0f && mn < mx) {
         const F2 D = add2(Lmx, neg2(Lmn));
         bool certain = false;
-        const float kf = round_certain(div22_parts(c.log2R, D),
-                                       k_err_bound(abs1(Lmx.hi), abs1(Lmn.hi), abs1(D.hi)), certain);
+        const float kf = round_certain_q(div22_parts_k(c.log2R, c.rcp_log2R, D),
+                                         k_err_num(abs1(Lmx.hi), abs1(Lmn.hi)), abs1(D.hi), certain);
         if (!certain) doubt = kf;
         k = kf < c.cap ? kf : c.cap;
     }
     if (Lmx.hi != 0.0f) {
         bool certain = false;
-        const F2 num = Lmx.hi < 0.0f ? c.guard_lo : c.guard_hi;
-        const float kg = round_certain(div22_parts(num, Lmx),
-                                       k_err_bound(abs1(Lmx.hi), 0.0f, abs1(Lmx.hi)), certain);
+        const bool neg = Lmx.hi < 0.0f;
+        const float kg = round_certain_q(div22_parts_k(neg ? c.guard_lo : c.guard_hi,
+                                                       neg ? c.rcp_guard_lo : c.rcp_guard_hi, Lmx),
+                                         k_err_num(abs1(Lmx.hi), 0.0f), abs1(Lmx.hi), certain);
         if (!certain && kg < doubt) doubt = kg;
         k = kg < k ? kg : k;
     }

@@ -170,7 +170,7 @@ struct DequantGroup {
 
 __device__ __forceinline__ DequantGroup dequant_group(float S, float k, const df::Tables& t) {
     DequantGroup d;
-    const df::F2 rkd = df::div21(df::F2{1.0f, 0.0f}, k);
+    const df::F2 rkd = df::recip21(k);
     d.rk_hi = rkd.hi;
     d.rk_lo = rkd.lo;
     if (!(S > 0.0f)) {

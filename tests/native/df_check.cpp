@@ -70,7 +70,7 @@ int main() {
         const int code = 1 + (int)(125 * U(rng));
         const float S = (float)std::exp2(-120.0 + 130.0 * U(rng));
         const float k = (float)(1.0 + 7.0 * U(rng));
-        const F2 rkd = coat::df::div21(F2{1.0f, 0.0f}, k);
+        const F2 rkd = coat::df::recip21(k);
         const F2 A = coat::df::add2(coat::df::log2_df(S, t), l448);
         const F2 L = {u2f(kLog2Frac448Hi[code]), u2f(kLog2Frac448Lo[code])};
         const F2 z = coat::df::mul22(coat::df::add2(L, A), rkd);
@@ -87,7 +87,7 @@ int main() {
         if (!(mnv > 0)) continue;
         const F2 Lmx = coat::df::log2_df(mxv, t), Lmn = coat::df::log2_df(mnv, t);
         const F2 D = coat::df::add2(Lmx, coat::df::neg2(Lmn));
-        const F2 q = coat::df::div22_parts(l2R, D);
+        const F2 q = coat::df::div22_parts_k(l2R, u2f(kLog2RRcp), D);
         const long double kw = log2l(448.0L * 512.0L) / (log2l((long double)mxv) - log2l((long double)mnv));
         const double krel = (double)fabsl(((long double)q.hi + (long double)q.lo) / kw - 1.0L);
         const double kb = coat::df::k_err_bound(std::fabs(Lmx.hi), std::fabs(Lmn.hi), std::fabs(D.hi));

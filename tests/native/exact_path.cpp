@@ -34,7 +34,8 @@ int main() {
     std::memcpy(logr, kLog2Recip, sizeof(logr));
     for (int i = 0; i < 33; ++i) { e_hi[i] = u2f(kExp2FracHi[i]); e_lo[i] = u2f(kExp2FracLo[i]); }
     const coat::df::Tables t{logr, e_hi, e_lo};
-    const coat::df::KConsts kc{cdf(kLog2RDf), cdf(kGuardLoDf), cdf(kGuardHiDf), 8.0f,
+    const coat::df::KConsts kc{cdf(kLog2RDf), cdf(kGuardLoDf), cdf(kGuardHiDf),
+                               u2f(kLog2RRcp), u2f(kGuardLoRcp), u2f(kGuardHiRcp), 8.0f,
                                448.0 * 512.0, -125.0, 126.0};
     char kind[4];
     unsigned a = 0, b = 0, c = 0;
@@ -43,7 +44,7 @@ int main() {
             if (std::scanf("%u %u %u", &a, &b, &c) != 3) return 2;
             const unsigned mag = a & 0x7Fu;
             const float S = u2f(b), k = u2f(c);
-            const F2 rkd = coat::df::div21(F2{1.0f, 0.0f}, k);
+            const F2 rkd = coat::df::recip21(k);
             const F2 A = coat::df::add2(coat::df::log2_df(S, t), cdf(kLog2_448Df));
             const F2 L = {u2f(kLog2Frac448Hi[mag]), u2f(kLog2Frac448Lo[mag])};
             bool slow = false;

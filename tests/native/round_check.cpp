@@ -50,6 +50,23 @@ int main() {
         if (!certain) ++near_uncertain;
         else if (r != (float)x) ++near_certain_wrong;
     }
+    // the ratio form (bound num / den, compared without a division) at and
+    // around midpoints, den spread over the range the exponent rule gives
+    long q_wrong = 0, q_uncertain = 0;
+    for (int i = 0; i < 2000000; ++i) {
+        const float a = (float)std::exp2(-60.0 + 70.0 * U(rng));
+        const float b = std::nextafter(a, 2.0f * a);
+        const double mid = 0.5 * ((double)a + (double)b);
+        const float den = (float)std::exp2(-3.0 + 12.0 * U(rng));
+        const float num = eps * den;
+        const double t = (U(rng) - 0.5) * 6.0 * (double)eps;
+        const double x = mid * (1.0 + t);
+        const double v = x * (1.0 + (U(rng) - 0.5) * 1.9 * (double)eps);
+        bool certain = false;
+        const float r = coat::df::round_certain_q(split(v), num, den, certain);
+        if (!certain) ++q_uncertain;
+        else if (r != (float)x) ++q_wrong;
+    }
     // the float64 recomputations against libm on the same formulas
     long dq_diff = 0, k_diff = 0;
     for (int i = 0; i < 100000; ++i) {
@@ -66,8 +83,8 @@ int main() {
         if (coat::df::k_f64(mx, mn, 229376.0, 8.0, -125.0, 126.0) != (float)kk) ++k_diff;
     }
     std::printf("random_wrong=%ld random_uncertain_frac=%.3e near_n=%ld near_certain_wrong=%ld "
-                "near_uncertain_frac=%.3e dequant_diff=%ld k_diff=%ld\n",
+                "near_uncertain_frac=%.3e dequant_diff=%ld k_diff=%ld q_wrong=%ld q_uncertain_frac=%.3e\n",
                 wrong, (double)random_uncertain / random_n, near_n, near_certain_wrong,
-                (double)near_uncertain / near_n, dq_diff, k_diff);
+                (double)near_uncertain / near_n, dq_diff, k_diff, q_wrong, (double)q_uncertain / 2000000);
     return 0;
 }

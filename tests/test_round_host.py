@@ -27,6 +27,8 @@ def test_round_certain_is_never_wrong(tmp_path):
     assert stats["random_uncertain_frac"] < 1e-4        # about 2 eps / ulp = 2^-15
     assert stats["near_uncertain_frac"] > 0.2           # the uncertain branch is exercised
     assert stats["dequant_diff"] == 0 and stats["k_diff"] == 0
+    # the division-free form of the test used for k
+    assert stats["q_wrong"] == 0 and stats["q_uncertain_frac"] > 0.2
 
 
 def test_header_compiles_for_the_device(tmp_path):
