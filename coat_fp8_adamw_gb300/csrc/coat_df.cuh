@@ -244,15 +244,19 @@ COAT_HD F2 log2_df(float x, const Tables& t) {
 
 // 2^z for a double-float z as 2^n (m.hi + m.lo), with m.hi + m.lo in about
 // [0.7, 1.42] not yet rounded: the caller rounds m once and scales it by 2^n.
+// z.hi is a multiple of a power of two g <= 1/32 with |z.lo| <= g / 2 (a
+// normalized pair with |z.hi| < 2^19, or one whose high part had an integer
+// subtracted): then z.hi - n and z.hi - n - j/32 are exact multiples of g, so
+// the low part joins them in one FastTwoSum.
 COAT_HD F2 exp2_df_parts(F2 z, const Tables& t, int& n_out) {
     const float n = rint(z.hi);
-    const F2 f = two_sum(sub(z.hi, n), z.lo);      // |f| <= 0.5 + tiny
-    const float jf = rint(mul(f.hi, 32.0f));       // -16..16 for a normalized z
-    // clamped so that no input (even a non-normalized or non-finite one) can
-    // index outside the 33-entry table
+    const float fh = sub(z.hi, n);                 // exact, |fh| <= 0.5
+    const float jf = rint(mul(fh, 32.0f));         // -16..16
+    // clamped so that no input (even a non-finite one) can index outside the
+    // 33-entry table
     const int j0 = (int)jf;
     const int j = j0 < -16 ? -16 : (j0 > 16 ? 16 : j0);
-    const F2 r = fast_two_sum(sub(f.hi, mul(jf, 0.03125f)), f.lo);  // |r| <= 1/64
+    const F2 r = fast_two_sum(sub(fh, mul(jf, 0.03125f)), z.lo);   // |r| <= 1/64 + |z.lo|
     // a = r ln 2
     const F2 a = mul22(r, F2{kLn2Hi, kLn2Lo});
     // e^a - 1 = a + a^2/2 + a^3/6 + a^4/24 + a^5/120 (|a| < 0.011: next term < 2^-48)
