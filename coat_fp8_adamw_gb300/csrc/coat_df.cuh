@@ -100,6 +100,8 @@ COAT_HD float from_bits(uint32_t u) {
 // (two power-of-two factors so that n in [-252, 254] is covered; beyond that
 // range the result saturates to 0 or infinity for |x| in [0.5, 2)).
 COAT_HD float scale2(float x, int n) {
+    // one factor when 2^n is a normal float: the same single rounding
+    if (n >= -126 && n <= 127) return mul(x, from_bits((uint32_t)(n + 127) << 23));
     n = n < -252 ? -252 : (n > 254 ? 254 : n);
     const int n1 = n / 2, n2 = n - n / 2;
     return mul(mul(x, from_bits((uint32_t)(n1 + 127) << 23)), from_bits((uint32_t)(n2 + 127) << 23));
