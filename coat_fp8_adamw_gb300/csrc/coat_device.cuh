@@ -169,8 +169,10 @@ __device__ __forceinline__ df::KConsts k_consts() {
 // Fresh per-group parameters with k correctly rounded to fp32 (double-float
 // logs and quotient, rounded once when that is certain, float64 otherwise)
 // and S = 2^(k log2 max - log2 448) rounded once.
-__device__ __forceinline__ QuantParams quant_params_precise(float mx, float mn,
-                                                            const df::Tables& t) {
+// quant_params_logs takes the two logs formed by the caller: Lmx = log2 mx,
+// Lmn = log2 mn (or Lmx when mn is zero or not below mx).
+__device__ __forceinline__ QuantParams quant_params_logs(float mx, float mn, df::F2 Lmx, df::F2 Lmn,
+                                                         const df::Tables& t) {
     QuantParams q;
     if (!(mx > 0.0f)) {
         q.k = 1.0f;
@@ -178,8 +180,6 @@ __device__ __forceinline__ QuantParams quant_params_precise(float mx, float mn,
         q.inv_mx = 0.0f;
         return q;
     }
-    const df::F2 Lmx = df::log2_df(mx, t);
-    const df::F2 Lmn = (mn > 0.0f && mn < mx) ? df::log2_df(mn, t) : Lmx;
     bool slow = false;
     const float k = df::k_certain(mx, mn, Lmx, Lmn, k_consts(), slow);
     const df::F2 e = df::add2(df::mul21(Lmx, k), df::neg2(const_df(kLog2_448Df)));
@@ -187,6 +187,13 @@ __device__ __forceinline__ QuantParams quant_params_precise(float mx, float mn,
     q.S = df::exp2_df(e, t);
     q.inv_mx = __frcp_rn(mx);
     return q;
+}
+__device__ __forceinline__ QuantParams quant_params_precise(float mx, float mn,
+                                                            const df::Tables& t) {
+    if (!(mx > 0.0f)) return quant_params_logs(mx, mn, df::F2{0.0f, 0.0f}, df::F2{0.0f, 0.0f}, t);
+    const df::F2 Lmx = df::log2_df(mx, t);
+    const df::F2 Lmn = (mn > 0.0f && mn < mx) ? df::log2_df(mn, t) : Lmx;
+    return quant_params_logs(mx, mn, Lmx, Lmn, t);
 }
 
 // Scaled, expanded value y = 448 sign(x) (|x| / max)^k, ready for E4M3 rounding.

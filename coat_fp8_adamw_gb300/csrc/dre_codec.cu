@@ -66,9 +66,27 @@ __device__ __forceinline__ void quantize_tile(const QuantArgs& a, const float (&
             sj.mn[gl] = mn[0];
         }
         __syncthreads();
-        for (int j = threadIdx.x; j < Gm::kGpc; j += kThreads) {
-            const float gm = sj.mx[j];
-            QuantParams q = quant_params_precise(gm, nz_key_value(sj.mn[j]), tab);
+        // With a warp or less of jobs (G >= 128) two adjacent lanes take a
+        // group: each forms one of the two logs (max, smallest non-zero), so
+        // that their chains run side by side, and the even lane takes the
+        // other's by a shuffle and forms k, S and the rest (1-3 % faster; with
+        // more jobs the extra lanes cost more than the overlap saves).
+        constexpr int kPer = Gm::kGpc <= 32 ? 2 : 1;
+        static_assert(kPer == 1 || (2 * Gm::kGpc) % 32 == 0, "whole warps of job lanes");
+        for (int j2 = threadIdx.x; j2 < kPer * Gm::kGpc; j2 += kThreads) {
+            const int j = j2 / kPer;
+            const float gm = sj.mx[j], gmn = nz_key_value(sj.mn[j]);
+            QuantParams q;
+            if constexpr (kPer == 2) {
+                const bool lmin = (j2 & 1) != 0;
+                const float arg = lmin && gmn > 0.0f && gmn < gm ? gmn : gm;
+                const df::F2 L = gm > 0.0f ? df::log2_df(arg, tab) : df::F2{0.0f, 0.0f};
+                const df::F2 Lo = {__shfl_xor_sync(0xFFFFFFFFu, L.hi, 1), __shfl_xor_sync(0xFFFFFFFFu, L.lo, 1)};
+                if (lmin) continue;
+                q = quant_params_logs(gm, gmn, L, Lo, tab);
+            } else {
+                q = quant_params_precise(gm, gmn, tab);
+            }
             float pr = 1.0f;
             if (gm > 0.0f && gm < 1.17549435e-38f) {
                 pr = 16777216.0f;
