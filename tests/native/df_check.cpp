@@ -93,6 +93,16 @@ int main() {
         const double kb = coat::df::k_err_bound(std::fabs(Lmx.hi), std::fabs(Lmn.hi), std::fabs(D.hi));
         if (krel / kb > k_bound_ratio) k_bound_ratio = krel / kb;
     }
+    // x 2^n against ldexp rounded once to fp32, for every n in [-260, 260]
+    // (the one-factor path, the two-factor path, subnormal results, overflow)
+    long scale2_miss = 0;
+    for (int i = 0; i < 2000; ++i) {
+        const float x = (float)(0.5 + 1.5 * U(rng)) * (i & 1 ? -1.0f : 1.0f);
+        for (int n = -260; n <= 260; ++n) {
+            const float want = (float)std::ldexp((double)x, n < -252 ? -252 : (n > 254 ? 254 : n));
+            if (coat::df::scale2(x, n) != want) ++scale2_miss;
+        }
+    }
     // log2: absolute error of hi+lo against libm log2 in double
     double log2_max_abs = 0, log2_max_near1 = 0;
     const int N = 2000000;
@@ -139,9 +149,10 @@ int main() {
     }
     std::printf("log2_max_abs=%.3e log2_max_abs_near1=%.3e exp2_miss_frac=%.3e exp2_max_rel=%.3e "
                 "div_miss_frac=%.3e dot_miss_frac=%.3e reduce_inexact=%ld reduce_max=%.6e "
-                "log2_bound_ratio=%.4f dequant_bound_ratio=%.4f k_bound_ratio=%.4f log2_sig_max_abs=%.3e\n",
+                "log2_bound_ratio=%.4f dequant_bound_ratio=%.4f k_bound_ratio=%.4f log2_sig_max_abs=%.3e "
+                "scale2_miss=%ld\n",
                 log2_max_abs, log2_max_near1, (double)exp2_miss / exp2_n, exp2_max_rel,
                 (double)div_miss / N, (double)dot_miss / N, reduce_inexact, reduce_max,
-                log2_bound_ratio, dequant_bound_ratio, k_bound_ratio, log2_sig_max_abs);
+                log2_bound_ratio, dequant_bound_ratio, k_bound_ratio, log2_sig_max_abs, scale2_miss);
     return 0;
 }

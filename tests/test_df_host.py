@@ -41,6 +41,9 @@ def test_double_float_toolkit_accuracy(tmp_path):
     # over the largest errors of the values they bound
     assert 0.0 < stats["dequant_bound_ratio"] < 0.5
     assert 0.0 < stats["k_bound_ratio"] < 0.5
+    # x 2^n is the correctly rounded product for every exponent, subnormal
+    # results and the clamped range included
+    assert stats["scale2_miss"] == 0
     assert stats["exp2_miss_frac"] < 1e-5              # correctly rounded except near ties
     assert stats["exp2_max_rel"] <= 2.0 ** -24 * 1.0001
     assert stats["div_miss_frac"] < 1e-5
