@@ -45,6 +45,8 @@
 #include <cstddef>
 
 #include "coat_device.cuh"
+#include <type_traits>
+
 #include "coat_kernels.h"
 #include "coat_round.cuh"
 
@@ -157,6 +159,24 @@ __device__ __forceinline__ void reload_inputs(const StepArgs& a, int64_t b, bool
                 cw[e / 4] |= (uint32_t)q[b + e] << (8 * (e & 3));
             }
         }
+    }
+}
+
+// The same for both moments' codes at once.
+__device__ __forceinline__ void reload_inputs_both(const StepArgs& a, int64_t b, uint32_t* gw, uint32_t* cm,
+                                                   uint32_t* cv) {
+    if (b + kVec <= a.n) {
+        const uint4* gp = reinterpret_cast<const uint4*>(a.g + b);
+        const uint4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
+        const uint4 m = __ldg(reinterpret_cast<const uint4*>(a.mq + b));
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.vq + b));
+        gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
+        gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
+        cm[0] = m.x; cm[1] = m.y; cm[2] = m.z; cm[3] = m.w;
+        cv[0] = v.x; cv[1] = v.y; cv[2] = v.z; cv[3] = v.w;
+    } else {
+        reload_inputs(a, b, false, gw, cm);
+        reload_inputs(a, b, true, gw, cv);
     }
 }
 
@@ -705,7 +725,95 @@ step_kernel_cta(const StepArgs a) {
     constexpr int kT = (kCta % NGC == 0) ? kCta / NGC : 0;
     constexpr bool kAsym = kT >= 8 && L >= 4;
     static_assert(!kAsym || (32 % kT == 0 && kT * NGC == kCta), "a group's lanes within one warp");
-    for (int jt = tid; jt < (kAsym ? kCta : 4 * NGC); jt += kCta) {
+    constexpr bool kOwnGroup = kStatBlocks && L == 1 && kCta == NGC;
+    if constexpr (kOwnGroup) {
+        // G = 16: a thread holds one whole group and runs its four statistics
+        // itself: the windows formed once, its inputs read again once, each
+        // statistic's test specialised, and the four logs side by side.
+        const int ri = tid;
+        const GroupWin win = make_win(a, R.P(0, ri), fast_err(R.rkd(0, ri).hi), fast_err(R.rkd(1, ri).hi),
+                                      R.fmx(0, ri), R.fmn(0, ri), R.fmx(1, ri), R.fmn(1, ri), R.gmx(ri));
+        const uint32_t hol[4] = {R.holders(0, ri), R.holders(1, ri), R.holders(2, ri), R.holders(3, ri)};
+        uint32_t gw[8], cm[4], cv[4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) gw[i] = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { cm[i] = 0u; cv[i] = 0u; }
+        if ((hol[0] | hol[1] | hol[2] | hol[3]) != 0u) reload_inputs_both(a, base, gw, cm, cv);
+        float best[4];
+        const auto one = [&](auto sc) {
+            constexpr int St = decltype(sc)::value;
+            constexpr bool second = St >= 2, is_max = (St & 1) == 0;
+            constexpr int sm_ = second ? 1 : 0;
+            float bst = is_max ? 0.0f : kInf;
+            if (hol[St] != 0u) {
+                const CandTest ct = cand_test(win, St, a.omb1);
+                const F2 A = R.A(sm_, ri), rkd = R.rkd(sm_, ri);
+                const float S = R.S(sm_, ri);
+                const float* kst_at = reinterpret_cast<const float*>(a.meta + g_first + ri) + 2 * sm_ + 1;
+                const auto kst = [kst_at]() { return *kst_at; };
+                const float beta = second ? a.beta2 : a.beta1, omb = second ? a.omb2 : a.omb1;
+                float* vals = second ? sm_v[tid] : sm_m[tid];
+                const uint32_t* cw = second ? cv : cm;
+                uint32_t msk = 0u, zm = 0u;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 x4 = *reinterpret_cast<const float4*>(vals + chunk_slot(tid, q));
+                    const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float ax = fabsf(xs[i]);
+                        bool in;
+                        if constexpr (is_max) {
+                            in = ax >= ct.hi;
+                        } else if constexpr (second) {
+                            in = ax <= fmaxf(ct.a0, 0.0f);
+                        } else {
+                            const float Tj = fmaf(ct.c, fabsf(bf16_of(gw, 4 * q + i)), ax);
+                            in = ax <= fmaxf(fmaf(ct.a1, Tj, ct.a0), ct.a2 * Tj);
+                        }
+                        msk |= (in ? 1u : 0u) << (4 * q + i);
+                        zm |= (ax == 0.0f ? 1u : 0u) << (4 * q + i);
+                    }
+                }
+                // a max window admits zeros only when degenerate; a zero is a
+                // candidate only when its inputs are not both zero
+                if constexpr (is_max) {
+                    if (ct.hi > 0.0f) zm = 0u;
+                }
+                uint32_t zc = msk & zm;
+                while (zc) {
+                    const int e = __ffs(zc) - 1;
+                    zc &= zc - 1u;
+                    if (bf16_of(gw, e) == 0.0f && (byte_of(cw, e) & 0x7Fu) == 0u) msk &= ~(1u << e);
+                }
+                while (msk) {
+                    const int e = __ffs(msk) - 1;
+                    msk &= msk - 1u;
+                    const float x = exact_moment(byte_of(cw, e), bf16_of(gw, e), second, A, rkd, S, kst, beta,
+                                                 omb, tab, lg_hi, lg_lo);
+                    vals[chunk_slot(tid, e >> 2) + (e & 3)] = x;   // encoded from the exact value
+                    const float ax = fabsf(x);
+                    if (is_max) bst = fmaxf(bst, ax);
+                    else if (ax > 0.0f) bst = fminf(bst, ax);
+                }
+            }
+            best[St] = (bst < kInf) ? bst : 0.0f;
+        };
+        one(std::integral_constant<int, 0>{});
+        one(std::integral_constant<int, 2>{});
+        one(std::integral_constant<int, 1>{});
+        one(std::integral_constant<int, 3>{});
+        F2 lx[4];
+#pragma unroll
+        for (int st = 0; st < 4; ++st) lx[st] = best[st] > 0.0f ? df::log2_df(best[st], tab) : F2{0.0f, 0.0f};
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+            R.ex(st, ri) = best[st];
+            R.lex(st, ri) = lx[st];
+        }
+    }
+    for (int jt = tid; jt < (kOwnGroup ? 0 : (kAsym ? kCta : 4 * NGC)); jt += kCta) {
         const int j = jt;
         int jg, s, sub = 0, nsub = 1;
         if constexpr (kAsym) {
